@@ -1,0 +1,223 @@
+/*
+ * ckv.h - C ABI of the GB300-native ClusterKV decode path.
+ *
+ * ClusterKV ("ClusterKV: Manipulating LLM KV Cache in Semantic Space for
+ * Recallable Compression", arXiv 2412.03213) recalls KV-cache tokens at the
+ * granularity of semantic clusters: the keys of each attention head are
+ * grouped by cosine K-means, every decode step scores the cluster centroids
+ * against the query, takes whole clusters in descending score order up to a
+ * token budget B, and runs attention over the selected, non-contiguous K/V.
+ *
+ * Terms used below
+ *   unit      one (sequence, layer, KV head); units are independent.
+ *   d         head dimension; this library is built for d = 128.
+ *   g         query heads sharing one KV head (GQA group), 1, 2, 4 or 8.
+ *   sinks     leading tokens never clustered and always attended (16).
+ *   L         prompt length; the prompt's clustered tokens are [sinks, L).
+ *   clustered_end   end of the clustered token range: L after prefill, then
+ *             +m after each incremental clustering.
+ *   pending   tokens [clustered_end, cur_len): generated but not yet
+ *             clustered; always attended.
+ *
+ * Buffers (all pointers are DEVICE pointers unless stated, 16-byte aligned,
+ * row-contiguous, owned by the caller; the library never frees them):
+ *   K, V      [units][max_len][d] of kv_dtype.  Row t of unit u starts at
+ *             element (u * max_len + t) * d.
+ *   q         [units][g][d] of kv_dtype (q_dtype must equal kv_dtype).
+ *   labels    [units][L - sinks] int32.
+ *   scores    [units][n_clusters] float.
+ *   idx       [units][B] int32; count [units] int32.
+ *   out       [units][g][d] float.
+ * The library owns the cluster state (centroids, sizes, prefix offsets, the
+ * label-sorted token permutation) and a workspace, all allocated on the
+ * device current at ckv_create and freed by ckv_destroy.
+ *
+ * Calls are asynchronous on the given stream (a cudaStream_t passed as
+ * void*, NULL = legacy default stream).  Argument, dtype, alignment and
+ * capacity errors are detected on the host before any launch and returned;
+ * nothing is launched then.  Device-side checks (an index out of range) set
+ * a device error word instead of trapping; ckv_get_device_error reads it.
+ * Bounded device waits that give up report CKV_ERR_TIMEOUT the same way.
+ * One context must not be used from two streams at the same time.
+ */
+#ifndef CKV_H
+#define CKV_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct ckv_ctx ckv_ctx;
+
+typedef enum {
+    CKV_OK = 0,
+    CKV_ERR_ARG = -1,           /* bad argument (null, out of range, wrong shape) */
+    CKV_ERR_DTYPE = -2,         /* unsupported or mismatched dtype */
+    CKV_ERR_CAPACITY = -3,      /* exceeds a capacity fixed at ckv_create */
+    CKV_ERR_CUDA = -4,          /* a CUDA runtime call failed */
+    CKV_ERR_TIMEOUT = -5,       /* a bounded device wait gave up */
+    CKV_ERR_DEVICE_CHECK = -6,  /* a device-side check failed (see ckv_get_device_error) */
+    CKV_ERR_UNIMPLEMENTED = -7, /* configuration not supported by this build */
+    CKV_ERR_ALIGN = -8,         /* pointer not 16-byte aligned */
+    CKV_ERR_STATE = -9          /* call out of order (e.g. select before clustering) */
+} ckv_status;
+
+typedef enum { CKV_F32 = 0, CKV_BF16 = 1 } ckv_dtype;
+
+/* Device error word values (ckv_get_device_error). */
+enum {
+    CKV_DEV_OK = 0,
+    CKV_DEV_TIMEOUT = 1,        /* an mbarrier wait ran past its iteration limit */
+    CKV_DEV_BAD_INDEX = 2,      /* a selected token index outside [0, cur_len) */
+    CKV_DEV_BAD_COUNT = 3,      /* a count outside [0, B] */
+    CKV_DEV_BAD_LABEL = 4,      /* a label outside [0, n_clusters) (treated as 0) */
+    CKV_DEV_BAD_CSR = 5         /* cluster offsets pointing outside the token permutation */
+};
+
+typedef struct {
+    int32_t units;        /* independent (sequence, layer, KV head) triples, >= 1 */
+    int32_t d;            /* head dimension; must be 128 */
+    int32_t g;            /* query heads per KV head: 1, 2, 4 or 8 */
+    int32_t sinks;        /* attention-sink tokens (ClusterKV: 16) */
+    int32_t ratio;        /* prompt tokens per cluster (ClusterKV: 80) */
+    int32_t m;            /* incremental clustering period (ClusterKV: 320) */
+    int32_t c_plus;       /* clusters per incremental clustering (ClusterKV: 4) */
+    int32_t iters;        /* Lloyd iterations per clustering (10) */
+    int32_t max_len;      /* tokens per unit in the caller's K/V buffers */
+    int32_t max_clusters; /* centroid capacity per unit (prefill + incremental) */
+    int32_t max_budget;   /* largest B passed to ckv_select / ckv_sparse_decode_attn */
+    int32_t kv_dtype;     /* ckv_dtype of K, V and q */
+} ckv_config;
+
+typedef struct {
+    int32_t n_clusters;       /* clusters per unit now (prefill + incremental) */
+    int32_t prefill_clusters; /* clusters made by the last ckv_cluster_prefill */
+    int32_t prefill_len;      /* L of the last ckv_cluster_prefill */
+    int32_t clustered_end;    /* end of the clustered token range */
+} ckv_info;
+
+/* Human-readable name of a ckv_status value (static string). */
+const char* ckv_status_str(int32_t status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int32_t ckv_version(void);
+
+/* Validates cfg and allocates the cluster state and workspace on the current
+ * device.  *out receives the context; on error *out is NULL and nothing stays
+ * allocated.  Errors: CKV_ERR_ARG (null, d != 128, g not in {1,2,4,8},
+ * sizes <= 0), CKV_ERR_DTYPE, CKV_ERR_CUDA (allocation failed). */
+ckv_status ckv_create(const ckv_config* cfg, ckv_ctx** out);
+
+/* Frees everything ckv_create allocated.  Synchronises the device first. */
+ckv_status ckv_destroy(ckv_ctx* ctx);
+
+/* Prefill clustering (ClusterKV page, section "Clustering in semantic space":
+ * clustering process, Fig. 4, and clustering strategy during inference).
+ * For every unit: keep tokens [0, sinks) as attention sinks; seed
+ * n_clusters centroids with the keys at stride s = min(ratio, n / n_clusters)
+ * of the n = L - sinks clustered keys; then run `iters` Lloyd iterations of
+ * (assignment to the centroid of largest cosine similarity, ties to the
+ * lower index) and (centroid = mean of the raw assigned keys, an empty
+ * cluster keeping its centroid).  The final assignment becomes the cluster
+ * metadata: sizes, prefix offsets and the token ids sorted by label (section
+ * "Selection and indexing mechanism", Fig. 8).  Replaces any earlier state.
+ * n_clusters = 0 selects (L - sinks) / ratio.
+ * Errors: CKV_ERR_ARG (L <= sinks, L > max_len, n_clusters > L - sinks),
+ * CKV_ERR_CAPACITY (n_clusters > max_clusters), CKV_ERR_ALIGN. */
+ckv_status ckv_cluster_prefill(ckv_ctx* ctx, const void* K, int32_t L, int32_t n_clusters,
+                               void* stream);
+
+/* Incremental clustering (section "Clustering in semantic space": every m
+ * decode steps the m newest keys are clustered among themselves into C+
+ * clusters, never together with the prompt's keys).  Clusters the keys of
+ * tokens [start, start + m) of every unit into c_plus new clusters with the
+ * same seeding (stride min(ratio, m / c_plus)) and Lloyd iterations, and
+ * appends their centroids and CSR segments after the existing ones.  start
+ * must equal the current clustered_end, which then advances by m.
+ * Errors: CKV_ERR_STATE (no prefill yet, start != clustered_end),
+ * CKV_ERR_ARG (m < c_plus, start + m > max_len, m > 400, c_plus > 16),
+ * CKV_ERR_CAPACITY (n_clusters + c_plus > max_clusters). */
+ckv_status ckv_cluster_incremental(ckv_ctx* ctx, const void* K, int32_t start, int32_t m,
+                                   int32_t c_plus, void* stream);
+
+/* One assignment step with the context's current n_clusters centroids:
+ * labels[u][i] = argmax_c cos(k_{sinks+i}, mu_c) for i < L - sinks, ties to
+ * the lower index (section "Clustering in semantic space", clustering
+ * process).  The cosine is taken against the centroid direction rounded to
+ * the operand type (bf16 for bf16 keys).  Does not change the state. */
+ckv_status ckv_kmeans_assign(ckv_ctx* ctx, const void* K, int32_t L, int32_t* labels,
+                             void* stream);
+
+/* One update step from caller-given labels (same layout as above, each in
+ * [0, n_clusters)): builds sizes, prefix offsets and the label-sorted token
+ * permutation of tokens [sinks, L), and sets every centroid with a non-empty
+ * cluster to the mean of its raw keys (section "Clustering in semantic
+ * space", clustering process; section "Semantic clustering optimisation",
+ * Fig. 7).  Sums are per cluster in a fixed order (deterministic, no float
+ * atomics).  Sets clustered_end = L and prefill_len = L. */
+ckv_status ckv_kmeans_update(ckv_ctx* ctx, const void* K, int32_t L, const int32_t* labels,
+                             void* stream);
+
+/* Centroid scores (section "Selection at semantic-cluster granularity"):
+ * scores[u][c] = sum over the g query heads h of q_h . mu_c (inner product,
+ * not cosine).  For bf16 the centroids are read as bf16; sums are fp32. */
+ckv_status ckv_score(ckv_ctx* ctx, const void* q, int32_t q_dtype, float* scores, void* stream);
+
+/* Selection and indexing from given scores (section "Selection and indexing
+ * mechanism", Fig. 8): rank clusters by (score descending, index ascending),
+ * prefix-sum their sizes in that order, take every cluster that starts before
+ * the budget and trim the last one.  idx[u][0..count) receives the token ids
+ * in rank order, ascending inside a cluster (the trimmed cluster keeps its
+ * lowest ids); count[u] = min(B, clustered tokens).  Entries past count are
+ * left unchanged.  Errors: CKV_ERR_STATE (no clusters), CKV_ERR_ARG (B < 0),
+ * CKV_ERR_CAPACITY (B > max_budget). */
+ckv_status ckv_select_scored(ckv_ctx* ctx, const float* scores, int32_t B, int32_t* idx,
+                             int32_t* count, void* stream);
+
+/* ckv_score followed by ckv_select_scored (scores kept in the workspace). */
+ckv_status ckv_select(ckv_ctx* ctx, const void* q, int32_t q_dtype, int32_t B, int32_t* idx,
+                      int32_t* count, void* stream);
+
+/* Sparse decode attention (section "Background": softmax(q K_S^T / sqrt(d))
+ * V_S).  For every unit and query head h: o_h = softmax over the attended
+ * set S of (q_h . k_t / sqrt(d)) times v_t, where S = sinks [0, sinks) +
+ * pending [clustered_end, cur_len) + idx[u][0..count[u]).  Each K/V row is
+ * read once for all g heads; fp32 arithmetic; out is fp32.  An index outside
+ * [0, cur_len) is skipped and sets CKV_DEV_BAD_INDEX.  Errors: CKV_ERR_ARG
+ * (cur_len < clustered_end or > max_len), CKV_ERR_CAPACITY (B > max_budget or
+ * more than 2*m pending tokens). */
+ckv_status ckv_sparse_decode_attn(ckv_ctx* ctx, const void* q, int32_t q_dtype, const void* K,
+                                  const void* V, const int32_t* idx, const int32_t* count,
+                                  int32_t B, int32_t cur_len, float* out, void* stream);
+
+/* Host-side copy of the context's counters. */
+ckv_status ckv_get_info(ckv_ctx* ctx, ckv_info* info);
+
+/* Copies the cluster state out to caller device buffers (any may be NULL):
+ * mu [units][n_clusters][d] float centroids; mu_hat [units][n_clusters][d]
+ * normalised centroid directions in the assignment operand type (bf16 for
+ * bf16 keys, else float); sizes [units][n_clusters]; offsets
+ * [units][n_clusters + 1]; perm [units][clustered_end - sinks]. */
+ckv_status ckv_export_clusters(ckv_ctx* ctx, float* mu, void* mu_hat, int32_t* sizes,
+                               int32_t* offsets, int32_t* perm, void* stream);
+
+/* Replaces the cluster state from caller device buffers (same layouts as
+ * ckv_export_clusters).  mu is required and the derived operand copies are
+ * recomputed from it; sizes, offsets and perm may all be NULL (centroids only,
+ * e.g. before ckv_kmeans_assign), else all three are required and
+ * clustered_end gives the perm length (+ sinks). */
+ckv_status ckv_import_clusters(ckv_ctx* ctx, int32_t n_clusters, int32_t clustered_end,
+                               const float* mu, const int32_t* sizes, const int32_t* offsets,
+                               const int32_t* perm, void* stream);
+
+/* Synchronises the context's last stream and reads then clears the device
+ * error word (CKV_DEV_*). */
+ckv_status ckv_get_device_error(ckv_ctx* ctx, int32_t* code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CKV_H */

@@ -1,0 +1,193 @@
+"""Thin ctypes binding of libckv.so (the C ABI declared in include/ckv.h).
+
+Argument marshalling only: tensors become device pointers, the current torch
+stream becomes the cudaStream_t, and a non-zero ckv_status becomes CKVError.
+Every step of the path runs in the library's CUDA kernels; there is no CPU
+fallback, and the library is loaded on first use (RuntimeError if it has not
+been built).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libckv.so")
+
+F32, BF16 = 0, 1
+DEV_ERRORS = {0: "ok", 1: "timeout", 2: "bad index", 3: "bad count", 4: "bad label", 5: "bad csr"}
+
+# Every entry point of include/ckv.h with its argument types.
+_P, _I, _F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float
+SIGNATURES = {
+    "ckv_status_str": ([_I], ctypes.c_char_p),
+    "ckv_version": ([], _I),
+    "ckv_create": ([_P, ctypes.POINTER(_P)], _I),
+    "ckv_destroy": ([_P], _I),
+    "ckv_cluster_prefill": ([_P, _P, _I, _I, _P], _I),
+    "ckv_cluster_incremental": ([_P, _P, _I, _I, _I, _P], _I),
+    "ckv_kmeans_assign": ([_P, _P, _I, _P, _P], _I),
+    "ckv_kmeans_update": ([_P, _P, _I, _P, _P], _I),
+    "ckv_score": ([_P, _P, _I, _P, _P], _I),
+    "ckv_select_scored": ([_P, _P, _I, _P, _P, _P], _I),
+    "ckv_select": ([_P, _P, _I, _I, _P, _P, _P], _I),
+    "ckv_sparse_decode_attn": ([_P, _P, _I, _P, _P, _P, _P, _I, _I, _P, _P], _I),
+    "ckv_get_info": ([_P, _P], _I),
+    "ckv_export_clusters": ([_P, _P, _P, _P, _P, _P, _P], _I),
+    "ckv_import_clusters": ([_P, _I, _I, _P, _P, _P, _P, _P], _I),
+    "ckv_get_device_error": ([_P, ctypes.POINTER(_I)], _I),
+}
+
+
+class Config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "units", "d", "g", "sinks", "ratio", "m", "c_plus", "iters", "max_len",
+        "max_clusters", "max_budget", "kv_dtype")]
+
+
+class Info(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "n_clusters", "prefill_clusters", "prefill_len", "clustered_end")]
+
+
+class CKVError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {lib().ckv_status_str(status).decode()}")
+
+
+_LIB = None
+
+
+def lib():
+    """The loaded libckv.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "recallable_kv_cache_gb300.build.build(); there is no CPU fallback")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.argtypes = args
+            fn.restype = res
+        _LIB = handle
+    return _LIB
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise CKVError(status, where)
+
+
+def ptr(t) -> int | None:
+    """Device pointer of a tensor (or None)."""
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+class Context:
+    """One library context: the cluster state of `units` (sequence, layer, KV
+    head) triples, allocated on the current CUDA device."""
+
+    def __init__(self, units: int, g: int, max_len: int, max_clusters: int, max_budget: int,
+                 kv_dtype: str = "bf16", d: int = 128, sinks: int = 16, ratio: int = 80,
+                 m: int = 320, c_plus: int = 4, iters: int = 10):
+        self.cfg = Config(units, d, g, sinks, ratio, m, c_plus, iters, max_len, max_clusters,
+                          max_budget, BF16 if kv_dtype == "bf16" else F32)
+        h = ctypes.c_void_p()
+        _check(lib().ckv_create(ctypes.byref(self.cfg), ctypes.byref(h)), "ckv_create")
+        self.handle = h
+
+    def close(self):
+        if getattr(self, "handle", None):
+            _check(lib().ckv_destroy(self.handle), "ckv_destroy")
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # -- clustering ------------------------------------------------------------
+    def cluster_prefill(self, K, L: int, n_clusters: int = 0, stream=None):
+        _check(lib().ckv_cluster_prefill(self.handle, ptr(K), L, n_clusters, _stream(stream)),
+               "ckv_cluster_prefill")
+
+    def cluster_incremental(self, K, start: int, m: int | None = None, c_plus: int | None = None,
+                            stream=None):
+        m = self.cfg.m if m is None else m
+        c_plus = self.cfg.c_plus if c_plus is None else c_plus
+        _check(lib().ckv_cluster_incremental(self.handle, ptr(K), start, m, c_plus, _stream(stream)),
+               "ckv_cluster_incremental")
+
+    def kmeans_assign(self, K, L: int, labels, stream=None):
+        _check(lib().ckv_kmeans_assign(self.handle, ptr(K), L, ptr(labels), _stream(stream)),
+               "ckv_kmeans_assign")
+
+    def kmeans_update(self, K, L: int, labels, stream=None):
+        _check(lib().ckv_kmeans_update(self.handle, ptr(K), L, ptr(labels), _stream(stream)),
+               "ckv_kmeans_update")
+
+    # -- decode ----------------------------------------------------------------
+    def score(self, q, scores, stream=None):
+        _check(lib().ckv_score(self.handle, ptr(q), _dtype_code(q), ptr(scores), _stream(stream)),
+               "ckv_score")
+
+    def select_scored(self, scores, B: int, idx, count, stream=None):
+        _check(lib().ckv_select_scored(self.handle, ptr(scores), B, ptr(idx), ptr(count),
+                                       _stream(stream)), "ckv_select_scored")
+
+    def select(self, q, B: int, idx, count, stream=None):
+        _check(lib().ckv_select(self.handle, ptr(q), _dtype_code(q), B, ptr(idx), ptr(count),
+                                _stream(stream)), "ckv_select")
+
+    def sparse_decode_attn(self, q, K, V, idx, count, B: int, cur_len: int, out, stream=None):
+        _check(lib().ckv_sparse_decode_attn(self.handle, ptr(q), _dtype_code(q), ptr(K), ptr(V),
+                                            ptr(idx), ptr(count), B, cur_len, ptr(out),
+                                            _stream(stream)), "ckv_sparse_decode_attn")
+
+    # -- state -----------------------------------------------------------------
+    def info(self) -> Info:
+        inf = Info()
+        _check(lib().ckv_get_info(self.handle, ctypes.byref(inf)), "ckv_get_info")
+        return inf
+
+    def export_clusters(self, mu=None, mu_hat=None, sizes=None, offsets=None, perm=None, stream=None):
+        _check(lib().ckv_export_clusters(self.handle, ptr(mu), ptr(mu_hat), ptr(sizes), ptr(offsets),
+                                         ptr(perm), _stream(stream)), "ckv_export_clusters")
+
+    def import_clusters(self, n_clusters: int, clustered_end: int, mu, sizes=None, offsets=None,
+                        perm=None, stream=None):
+        _check(lib().ckv_import_clusters(self.handle, n_clusters, clustered_end, ptr(mu), ptr(sizes),
+                                         ptr(offsets), ptr(perm), _stream(stream)),
+               "ckv_import_clusters")
+
+    def device_error(self) -> int:
+        v = ctypes.c_int32()
+        _check(lib().ckv_get_device_error(self.handle, ctypes.byref(v)), "ckv_get_device_error")
+        return v.value

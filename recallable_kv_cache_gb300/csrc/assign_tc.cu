@@ -1,0 +1,322 @@
+// K-means assignment on the fifth-generation tensor cores (ClusterKV page,
+// section "Clustering in semantic space", clustering process: every key joins
+// the centroid of largest cosine similarity; section "Semantic clustering
+// optimisation": the assignment is a batched keys x centroids product followed
+// by an arg-max).
+//
+// cos(k, mu_c) = (k . mu_hat_c) / ||k|| and ||k|| > 0 is the same for every c,
+// so the arg-max over c of k . mu_hat_c is the cosine arg-max: the key
+// normalisation is folded away and the raw bf16 keys feed the MMA directly.
+//
+// One persistent CTA per SM walks a contiguous range of 128-token tiles
+// (flattened over units).  Warp roles:
+//   warp 0     TMA producer: the unit's mu_hat [cpad x 128] once per unit
+//              (resident in smem), key tiles [128 x 128] through a ring;
+//   warp 1     TMEM owner and MMA issuer: per tile and per column chunk of at
+//              most 256 centroids, 8 x tcgen05.mma (K = 16 each) into one of
+//              two 256-column TMEM slots;
+//   warps 2-5  epilogue: tcgen05.ld of the fp32 dots (one TMEM lane = one
+//              token), running arg-max in increasing centroid order with a
+//              strict '>' (ties keep the lower index), label store.
+// All mbarrier waits are bounded; a timeout sets the device error word and
+// every role leaves its loop.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace ckv {
+namespace {
+
+constexpr int A_STAGE_BYTES = ASSIGN_TILE * D * 2;  // 32 KB: two 64-column panels
+constexpr int A_PANEL_BYTES = ASSIGN_TILE * 128;    // 16 KB
+constexpr int B_BOX_ROWS = 32;
+constexpr int THREADS = 192;
+
+struct AssignArgs {
+    int n;              // clustered tokens per unit
+    int C;              // centroids
+    int cpad;           // C rounded up to 32
+    int nchunk;         // column chunks per tile (ceil(cpad / 256))
+    int tiles_per_unit;
+    int total_tiles;
+    int tiles_per_cta;
+    int sinks;
+    int stages;
+    int32_t* labels;
+    int32_t* dev_err;
+};
+
+struct __align__(8) Bars {
+    uint64_t a_full[4];
+    uint64_t a_empty[4];
+    uint64_t b_full;
+    uint64_t b_empty;
+    uint64_t tm_full[2];
+    uint64_t tm_empty[2];
+    uint32_t tmem_base;
+    int abort;
+};
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Bars* bs,
+                                              int32_t* dev_err) {
+    if (ptx::mbar_wait(bar, parity, WAIT_LIMIT, &bs->abort)) return true;
+    if (atomicExch(&bs->abort, 1) == 0 && dev_err) atomicCAS(dev_err, 0, CKV_DEV_TIMEOUT);
+    return false;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    assign_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmMu,
+                     const AssignArgs p) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // 1024-byte alignment for the 128-byte swizzle atoms
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    unsigned char* A = smem;                                     // stages x 32 KB
+    unsigned char* Bm = smem + (size_t)p.stages * A_STAGE_BYTES;  // 2 panels x cpad x 128 B
+    Bars* bs = reinterpret_cast<Bars*>(Bm + (size_t)p.cpad * 256);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t_begin = blockIdx.x * p.tiles_per_cta;
+    const int t_end = min(p.total_tiles, t_begin + p.tiles_per_cta);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            ptx::mbar_init(&bs->a_full[s], 1);
+            ptx::mbar_init(&bs->a_empty[s], 1);
+        }
+        ptx::mbar_init(&bs->b_full, 1);
+        ptx::mbar_init(&bs->b_empty, 1);
+        for (int s = 0; s < 2; ++s) {
+            ptx::mbar_init(&bs->tm_full[s], 1);
+            ptx::mbar_init(&bs->tm_empty[s], 4);
+        }
+        bs->abort = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(&bs->tmem_base, 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = bs->tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            ptx::prefetch_tmap(&tmK);
+            ptx::prefetch_tmap(&tmMu);
+            int cur_unit = -1, b_loads = 0;
+            for (int t = t_begin, it = 0; t < t_end; ++t, ++it) {
+                const int u = t / p.tiles_per_unit, tl = t % p.tiles_per_unit;
+                if (u != cur_unit) {
+                    if (cur_unit >= 0 && !wait_or_abort(&bs->b_empty, (b_loads - 1) & 1, bs, p.dev_err))
+                        break;
+                    ptx::mbar_arrive_expect_tx(&bs->b_full, (uint32_t)p.cpad * 256u);
+                    for (int pn = 0; pn < 2; ++pn)
+                        for (int r0 = 0; r0 < p.cpad; r0 += B_BOX_ROWS)
+                            ptx::tma_load_3d(Bm + (size_t)pn * p.cpad * 128 + (size_t)r0 * 128, &tmMu,
+                                             pn * 64, r0, u, &bs->b_full);
+                    ++b_loads;
+                    cur_unit = u;
+                }
+                const int s = it % p.stages;
+                if (it >= p.stages &&
+                    !wait_or_abort(&bs->a_empty[s], ((it / p.stages) - 1) & 1, bs, p.dev_err))
+                    break;
+                unsigned char* a = A + (size_t)s * A_STAGE_BYTES;
+                ptx::mbar_arrive_expect_tx(&bs->a_full[s], A_STAGE_BYTES);
+                const int row = p.sinks + tl * ASSIGN_TILE;
+                ptx::tma_load_3d(a, &tmK, 0, row, u, &bs->a_full[s]);
+                ptx::tma_load_3d(a + A_PANEL_BYTES, &tmK, 64, row, u, &bs->a_full[s]);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t a_base = ptx::smem_u32(A);
+            const uint32_t b_base = ptx::smem_u32(Bm);
+            int cur_unit = -1, b_loads = 0, item = 0;
+            bool alive = true;
+            for (int t = t_begin, it = 0; t < t_end && alive; ++t, ++it) {
+                const int u = t / p.tiles_per_unit;
+                if (u != cur_unit) {
+                    if (cur_unit >= 0) ptx::mma_commit(&bs->b_empty);
+                    if (!wait_or_abort(&bs->b_full, b_loads & 1, bs, p.dev_err)) break;
+                    ++b_loads;
+                    cur_unit = u;
+                }
+                const int s = it % p.stages;
+                if (!wait_or_abort(&bs->a_full[s], (it / p.stages) & 1, bs, p.dev_err)) break;
+                ptx::tc_fence_after();
+                const uint32_t a_st = a_base + (uint32_t)s * A_STAGE_BYTES;
+                for (int ch = 0; ch < p.nchunk; ++ch, ++item) {
+                    const int slot = item & 1;
+                    if (item >= 2 &&
+                        !wait_or_abort(&bs->tm_empty[slot], ((item >> 1) - 1) & 1, bs, p.dev_err)) {
+                        alive = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const int ncols = min(256, p.cpad - 256 * ch);
+                    const uint32_t idesc = ptx::idesc_bf16_f32(128, ncols);
+                    const uint32_t d_tmem = tmem + (uint32_t)slot * 256u;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const uint32_t koff = (uint32_t)(k & 3) * 32u;
+                        const uint64_t ad = ptx::smem_desc_sw128(a_st + (uint32_t)(k >> 2) * A_PANEL_BYTES + koff);
+                        const uint64_t bd = ptx::smem_desc_sw128(
+                            b_base + (uint32_t)(k >> 2) * (uint32_t)p.cpad * 128u + (uint32_t)ch * 256u * 128u + koff);
+                        ptx::mma_bf16(d_tmem, ad, bd, idesc, k > 0 ? 1u : 0u);
+                    }
+                    ptx::mma_commit(&bs->tm_full[slot]);
+                }
+                ptx::mma_commit(&bs->a_empty[s]);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        int item = 0;
+        bool alive = true;
+        for (int t = t_begin; t < t_end && alive; ++t) {
+            const int u = t / p.tiles_per_unit, tl = t % p.tiles_per_unit;
+            float best = -INFINITY;
+            int arg = 0;
+            for (int ch = 0; ch < p.nchunk; ++ch, ++item) {
+                const int slot = item & 1;
+                const bool ok = __all_sync(
+                    0xffffffffu, wait_or_abort(&bs->tm_full[slot], (item >> 1) & 1, bs, p.dev_err));
+                if (!ok) {
+                    alive = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const int c0 = 256 * ch;
+                const int nvalid = min(256, p.C - c0);
+                const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)slot * 256u;
+                for (int g0 = 0; g0 < nvalid; g0 += 32) {
+                    uint32_t r[32];
+                    ptx::tmem_ld32(taddr + (uint32_t)g0, r);
+                    ptx::tmem_ld_wait();
+                    const int lim = nvalid - g0;
+                    if (lim >= 32) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const float v = __uint_as_float(r[j]);
+                            if (v > best) {
+                                best = v;
+                                arg = c0 + g0 + j;
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const float v = __uint_as_float(r[j]);
+                            if (j < lim && v > best) {
+                                best = v;
+                                arg = c0 + g0 + j;
+                            }
+                        }
+                    }
+                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&bs->tm_empty[slot]);
+            }
+            if (!alive) break;
+            const int row = tl * ASSIGN_TILE + q * 32 + lane;
+            if (row < p.n) p.labels[(size_t)u * p.n + row] = arg;
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (bs->abort) {
+        // let copies / MMAs already issued drain before TMEM is released
+        const long long t0 = clock64();
+        while (clock64() - t0 < 20000000LL) {
+        }
+    }
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 512);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// 3-D bf16 tensor [units][rows][128], box {64, box_rows, 1}, 128-byte swizzle.
+bool encode_3d(CUtensorMap* m, const void* base, int rows, int units, int box_rows) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)units};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)rows * D * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                     es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+size_t assign_tc_smem(int cpad, int* stages_out) {
+    const size_t fixed = (size_t)cpad * 256 + sizeof(Bars) + 1024;
+    const size_t cap = 232448;
+    int stages = 4;
+    while (stages > 2 && fixed + (size_t)stages * A_STAGE_BYTES > cap) --stages;
+    if (stages_out) *stages_out = stages;
+    return fixed + (size_t)stages * A_STAGE_BYTES;
+}
+
+cudaError_t launch_assign_tc(const ckv_ctx* ctx, const void* K, int n, int C, int32_t* labels,
+                             cudaStream_t s) {
+    const int cpad = round_up(C, 32);
+    int stages = 0;
+    const size_t smem = assign_tc_smem(cpad, &stages);
+    if (smem > 232448 || cpad > ctx->cmax_pad) return cudaErrorInvalidValue;
+    CUtensorMap tmK, tmMu;
+    if (!encode_3d(&tmK, K, ctx->cfg.max_len, ctx->cfg.units, ASSIGN_TILE)) return cudaErrorInvalidValue;
+    if (!encode_3d(&tmMu, ctx->mu_hat, ctx->cmax_pad, ctx->cfg.units, B_BOX_ROWS))
+        return cudaErrorInvalidValue;
+    AssignArgs a;
+    a.n = n;
+    a.C = C;
+    a.cpad = cpad;
+    a.nchunk = ceil_div(cpad, 256);
+    a.tiles_per_unit = ceil_div(n, ASSIGN_TILE);
+    a.total_tiles = a.tiles_per_unit * ctx->cfg.units;
+    const int grid = a.total_tiles < ctx->num_sms ? a.total_tiles : ctx->num_sms;
+    a.tiles_per_cta = ceil_div(a.total_tiles, grid);
+    const int used = ceil_div(a.total_tiles, a.tiles_per_cta);
+    a.sinks = ctx->cfg.sinks;
+    a.stages = stages;
+    a.labels = labels;
+    a.dev_err = ctx->dev_err;
+    cudaError_t e = cudaFuncSetAttribute(assign_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    assign_tc_kernel<<<used, THREADS, smem, s>>>(tmK, tmMu, a);
+    return cudaGetLastError();
+}
+
+}  // namespace ckv

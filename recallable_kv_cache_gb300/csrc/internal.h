@@ -1,0 +1,89 @@
+// Internal declarations shared by the C-ABI layer and the kernel files.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ckv.h"
+
+namespace ckv {
+
+constexpr int D = 128;             // head dimension this build supports
+constexpr int CSR_CHUNK = 1024;    // tokens per block in the CSR count/scatter passes
+constexpr int SEG_ROWS = 64;       // rows per centroid-update task
+constexpr int ASSIGN_TILE = 128;   // tokens per tcgen05 assignment tile (MMA M)
+constexpr int MAX_ASSIGN_CPAD = 640;  // centroid rows the assignment keeps resident in smem
+constexpr long long WAIT_LIMIT = 2000000000LL;  // SM cycles before a bounded wait gives up
+
+inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
+inline int ceil_div(int x, int m) { return (x + m - 1) / m; }
+
+}  // namespace ckv
+
+struct ckv_ctx {
+    ckv_config cfg;
+    int device;
+    int num_sms;
+    int cmax;        // centroid capacity per unit
+    int cmax_pad;    // rows of the assignment operand per unit (multiple of 16)
+    int ntok;        // max_len - sinks: capacity of labels / perm per unit
+    int nchunk;      // ceil(ntok / CSR_CHUNK)
+    int max_tasks;   // centroid-update tasks per unit
+    int max_splits;  // attention splits per unit
+    int attn_rows;   // rows an attention call may cover per unit
+    size_t elem;     // bytes per K/V element
+
+    int n_clusters;
+    int prefill_clusters;
+    int prefill_len;
+    int clustered_end;
+    cudaStream_t last_stream;
+
+    // state
+    float* mu32;        // [U][cmax][D] centroids (fp32 master)
+    void* mu_s;         // [U][cmax][D] scoring operand (bf16 copy, or == mu32 for f32)
+    void* mu_hat;       // [U][cmax_pad][D] normalised directions (bf16 or f32)
+    int32_t* sizes;     // [U][cmax]
+    int32_t* offsets;   // [U][cmax + 1]
+    int32_t* perm;      // [U][ntok]
+    // workspace
+    int32_t* labels;    // [U][ntok]
+    int32_t* chunk_cnt; // [U][nchunk][cmax]
+    int32_t* task_off;  // [U][cmax + 1]
+    int32_t* task_cl;   // [U][max_tasks]
+    float* seg_part;    // [U][max_tasks][D]
+    float* scores;      // [U][cmax]
+    float* attn_part;   // [U][max_splits][g * (D + 2)]
+    int32_t* attn_cnt;  // [U]
+    int32_t* dev_err;   // device error word
+};
+
+namespace ckv {
+
+// centroid operand copies for centroids [c0, c1) of every unit
+cudaError_t launch_shadows(const ckv_ctx* ctx, int c0, int c1, cudaStream_t s);
+// mu[j] = K[sinks + base + j * stride], j in [0, C), then shadows
+cudaError_t launch_seed(const ckv_ctx* ctx, const void* K, int C, int stride, cudaStream_t s);
+// labels[u][i] = argmax_c cos(k_{sinks+i}, mu_c), i < n
+cudaError_t launch_assign(const ckv_ctx* ctx, const void* K, int n, int C, int32_t* labels,
+                          cudaStream_t s);
+// CSR of labels over tokens [sinks, sinks+n) + centroid means + shadows
+cudaError_t launch_update(const ckv_ctx* ctx, const void* K, int n, int C, const int32_t* labels,
+                          cudaStream_t s);
+// incremental clustering of [start, start+m) into c_plus clusters appended at C_old
+cudaError_t launch_incremental(const ckv_ctx* ctx, const void* K, int start, int m, int c_plus,
+                               int C_old, int csr_base, cudaStream_t s);
+// scores[u][c] = sum_h q_h . mu_c, written with row stride `stride`
+cudaError_t launch_score(const ckv_ctx* ctx, const void* q, int C, float* scores, int stride,
+                         cudaStream_t s);
+cudaError_t launch_select(const ckv_ctx* ctx, const float* scores, int stride, int C, int B,
+                          int32_t* idx, int32_t* count, cudaStream_t s);
+// split-K sparse decode attention; partials/counters are caller-provided scratch
+cudaError_t launch_attention(const void* q, const void* K, const void* V, const int32_t* idx,
+                             const int32_t* count, int units, int g, int kv_dtype, int max_len,
+                             int sinks, int clustered_end, int cur_len, int B, float* out,
+                             float* part, int32_t* counters, int max_splits, int32_t* dev_err,
+                             int num_sms, cudaStream_t s);
+// rows of the attended set one attention CTA covers
+int attention_rows_per_split(int kv_dtype, int g);
+
+}  // namespace ckv

@@ -1,0 +1,179 @@
+"""GPU parity of the decode step (scoring, selection, sparse attention) against
+the CPU oracle, through the C ABI.  Each part gets the oracle's own upstream
+result as input so that errors do not cascade."""
+import numpy as np
+import pytest
+import torch
+
+import oracle.clusterkv as ck
+from parity import (ATTN_TOL, check_assignment, make_ctx, score_tol, to64, upload_state)
+from recallable_kv_cache_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+CASES = {
+    # name: (workload, units, L, C, B, pending)
+    "bf16_g4": ("layer_32k", 3, 16 + 1000, 13, 200, 37),
+    "f32_g1": ("tiny_2k", 1, 2048, 25, 256, 5),
+    "bf16_g4_c300": ("layer_32k", 2, 16 + 6000, 300, 1024, 320),
+}
+
+
+def build_case(name, seed_shift=0):
+    wname, U, L, C, B, pend = CASES[name]
+    w = synth.scaled(synth.WORKLOADS[wname], units=U, L=L, decode_steps=pend + 8, C=C, B=B,
+                     n_centres=C, seed=synth.WORKLOADS[wname].seed + seed_shift)
+    K, V = synth.make_kv(w)
+    Q = synth.make_queries(w, 3)
+    states = [ck.cluster_prefill(to64(K[u]), L, C, iters=3, operand="bf16" if w.dtype == "bf16" else "f64")
+              for u in range(U)]
+    for s in states:  # the GPU keeps fp32 centroids: the oracle uses the same values
+        s["mu"] = s["mu"].astype(np.float32).astype(np.float64)
+    return w, K, V, Q, states
+
+
+@pytest.fixture(scope="module", params=list(CASES))
+def case(request):
+    torch.cuda.init()
+    w, K, V, Q, states = build_case(request.param)
+    ctx = make_ctx(w.units, w.g, w.max_len, w.C + 8, max(w.B, 1024), w.dtype)
+    upload_state(ctx, states, w.L)
+    Kd, Vd = K.cuda().contiguous(), V.cuda().contiguous()
+    yield dict(w=w, K=K, V=V, Q=Q, states=states, ctx=ctx, Kd=Kd, Vd=Vd, name=request.param)
+    ctx.close()
+
+
+def test_score_parity(case):
+    w, ctx = case["w"], case["ctx"]
+    for qi in range(case["Q"].shape[0]):
+        q = case["Q"][qi]
+        sc = torch.empty(w.units, w.C, dtype=torch.float32, device="cuda")
+        ctx.score(q.cuda().contiguous(), sc)
+        got = to64(sc)
+        for u in range(w.units):
+            want = ck.score(to64(q[u]), case["states"][u]["mu"])
+            tol = score_tol(to64(q[u]), case["states"][u]["mu"], w.dtype)
+            assert (np.abs(got[u] - want) <= tol).all(), np.abs(got[u] - want).max()
+
+
+@pytest.mark.parametrize("B", [0, 1, 57, 200, 10 ** 9])
+def test_select_given_scores_bit_exact(case, B):
+    w, ctx = case["w"], case["ctx"]
+    B = min(B, 1024)
+    q = case["Q"][0]
+    sc = np.stack([ck.score(to64(q[u]), case["states"][u]["mu"]) for u in range(w.units)]).astype(np.float32)
+    idx = torch.full((w.units, max(B, 1)), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.empty(w.units, dtype=torch.int32, device="cuda")
+    ctx.select_scored(torch.from_numpy(sc).cuda(), B, idx, cnt)
+    idx, cnt = idx.cpu().numpy(), cnt.cpu().numpy()
+    for u in range(w.units):
+        st = case["states"][u]
+        want, wc = ck.select(sc[u].astype(np.float64), st["sizes"], st["offsets"], st["perm"], B)
+        assert cnt[u] == wc == min(B, w.L - 16)
+        assert np.array_equal(idx[u, :wc], want)
+        assert (idx[u, wc:] == -7).all()  # entries past count untouched
+
+
+def test_fused_select_equals_score_then_select(case):
+    w, ctx = case["w"], case["ctx"]
+    q = case["Q"][1].cuda().contiguous()
+    sc = torch.empty(w.units, w.C, dtype=torch.float32, device="cuda")
+    ctx.score(q, sc)
+    i1 = torch.empty(w.units, w.B, dtype=torch.int32, device="cuda")
+    c1 = torch.empty(w.units, dtype=torch.int32, device="cuda")
+    i2, c2 = torch.empty_like(i1), torch.empty_like(c1)
+    ctx.select_scored(sc, w.B, i1, c1)
+    ctx.select(q, w.B, i2, c2)
+    assert torch.equal(c1, c2) and torch.equal(i1, i2)
+
+
+@pytest.mark.parametrize("pending", [0, 1, "case"])
+def test_attention_given_idx(case, pending):
+    w, ctx = case["w"], case["ctx"]
+    pend = CASES[case["name"]][5] if pending == "case" else pending
+    cur_len = w.L + pend
+    for qi in range(2):
+        q = case["Q"][qi]
+        sc = np.stack([ck.score(to64(q[u]), case["states"][u]["mu"]) for u in range(w.units)])
+        idx = np.zeros((w.units, w.B), dtype=np.int32)
+        cnt = np.zeros(w.units, dtype=np.int32)
+        for u in range(w.units):
+            st = case["states"][u]
+            sel, c = ck.select(sc[u], st["sizes"], st["offsets"], st["perm"], w.B)
+            idx[u, :c], cnt[u] = sel, c
+        out = torch.empty(w.units, w.g, 128, dtype=torch.float32, device="cuda")
+        ctx.sparse_decode_attn(q.cuda().contiguous(), case["Kd"], case["Vd"], torch.from_numpy(idx).cuda(),
+                               torch.from_numpy(cnt).cuda(), w.B, cur_len, out)
+        got = to64(out)
+        for u in range(w.units):
+            toks = ck.attention_tokens(16, w.L, cur_len, idx[u, :cnt[u]])
+            want = ck.sparse_attention(to64(q[u]), to64(case["K"][u]), to64(case["V"][u]), toks)
+            err = np.abs(got[u] - want).max()
+            assert err <= ATTN_TOL[w.dtype], err
+        assert ctx.device_error() == 0
+
+
+def test_budget_covering_everything_is_full_attention(case):
+    """B >= clustered tokens: the sparse set is every token (sinks, clustered,
+    pending), so the result equals full attention."""
+    w, ctx = case["w"], case["ctx"]
+    B = 1024
+    if w.L - 16 > B:
+        pytest.skip("more clustered tokens than the largest budget of this case")
+    q = case["Q"][2].cuda().contiguous()
+    idx = torch.empty(w.units, B, dtype=torch.int32, device="cuda")
+    cnt = torch.empty(w.units, dtype=torch.int32, device="cuda")
+    ctx.select(q, B, idx, cnt)
+    cur_len = w.L + 3
+    out = torch.empty(w.units, w.g, 128, dtype=torch.float32, device="cuda")
+    ctx.sparse_decode_attn(q, case["Kd"], case["Vd"], idx, cnt, B, cur_len, out)
+    got = to64(out)
+    for u in range(w.units):
+        want = ck.full_attention(to64(case["Q"][2][u]), to64(case["K"][u]), to64(case["V"][u]), cur_len)
+        assert np.abs(got[u] - want).max() <= ATTN_TOL[w.dtype]
+
+
+def test_bad_index_is_reported_not_faulted(case):
+    w, ctx = case["w"], case["ctx"]
+    q = case["Q"][0].cuda().contiguous()
+    idx = torch.randint(16, w.L, (w.units, w.B), dtype=torch.int32, device="cuda")
+    idx[:, 3] = w.max_len + 1000  # outside [0, cur_len)
+    idx[:, 4] = -5
+    cnt = torch.full((w.units,), w.B, dtype=torch.int32, device="cuda")
+    out = torch.empty(w.units, w.g, 128, dtype=torch.float32, device="cuda")
+    assert ctx.device_error() == 0
+    ctx.sparse_decode_attn(q, case["Kd"], case["Vd"], idx, cnt, w.B, w.L, out)
+    assert ctx.device_error() == 2  # CKV_DEV_BAD_INDEX
+    assert torch.isfinite(out).all()
+    # the skipped rows are excluded from the softmax
+    toks_ok = idx.cpu().numpy()
+    for u in range(w.units):
+        keep = toks_ok[u][(toks_ok[u] >= 0) & (toks_ok[u] < w.L)]
+        want = ck.sparse_attention(to64(case["Q"][0][u]), to64(case["K"][u]), to64(case["V"][u]),
+                                   ck.attention_tokens(16, w.L, w.L, keep))
+        assert np.abs(to64(out)[u] - want).max() <= ATTN_TOL[w.dtype]
+
+
+def test_select_ties_and_empty_clusters():
+    """Hand-made CSR with empty clusters and tied scores (including -0.0):
+    ranks by (score desc, index asc), skips empty clusters, trims the last."""
+    torch.cuda.init()
+    U, d, C, L = 2, 128, 7, 16 + 20
+    ctx = make_ctx(U, 1, L + 8, C, 64, "f32")
+    rng = np.random.default_rng(0)
+    sizes = np.array([3, 0, 5, 2, 0, 6, 4], dtype=np.int32)
+    offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    perm = (16 + rng.permutation(20)).astype(np.int32)
+    st = dict(mu=rng.standard_normal((C, d)), sizes=sizes, offsets=offsets, perm=perm)
+    upload_state(ctx, [st, st], L)
+    scores = np.array([[1.0, 5.0, 1.0, -0.0, 9.0, 0.0, 1.0],
+                       [-1.0, -1.0, -2.0, -1.0, -3.0, -1.0, -1.0]], dtype=np.float32)
+    for B in (0, 1, 3, 4, 9, 13, 20, 64):
+        idx = torch.full((U, max(B, 1)), -1, dtype=torch.int32, device="cuda")  # [units][B]
+        cnt = torch.empty(U, dtype=torch.int32, device="cuda")
+        ctx.select_scored(torch.from_numpy(scores).cuda(), B, idx, cnt)
+        for u in range(U):
+            want, wc = ck.select(scores[u].astype(np.float64), sizes, offsets, perm, B)
+            assert cnt[u].item() == wc
+            assert np.array_equal(idx[u, :wc].cpu().numpy(), want)
+    ctx.close()
