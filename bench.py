@@ -1,0 +1,442 @@
+#!/usr/bin/env python
+"""Throughput of the ClusterKV decode path on one GB300 (or N, one process each).
+
+One bench step is one whole ClusterKV job of the 32k decode workload: 32 layers
+x 8 KV heads (256 units), head dim 128, GQA 4, bf16, a 32768-token prompt:
+  * prefill clustering of every unit (C = 409, 10 Lloyd iterations);
+  * 1024 decode steps, each: centroid scoring, cluster selection (B = 1024),
+    sparse attention over sinks + pending + selected tokens; incremental
+    clustering of the 320 newest tokens into 4 clusters before steps 320, 640
+    and 960.
+Inputs (keys, values, the 1024 queries of every unit) are generated on the
+device before the timed region.  value = decode tokens of the job / job time
+(clustering included); the per-phase numbers are extra keys.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from recallable_kv_cache_gb300 import synth  # noqa: E402
+
+METRIC = "sparse-decode tokens/s at 32k ctx, B=1024; K-means ms/layer; % of HBM roofline"
+WORKLOAD = "decode_32k"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=5)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=WORKLOAD)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d.get("hbm_gbs", 6800.0), "measured", d
+    return 6800.0, "fallback", {}
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.index is not None:
+            cmd += ["-i", str(self.index)]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- events in graphs
+class ExternalEvents:
+    """cudaEventRecordWithFlags(..., cudaEventRecordExternal) so that event
+    records captured into a CUDA graph become timing nodes of the graph."""
+
+    def __init__(self):
+        path = None
+        for line in open("/proc/self/maps"):
+            if "libcudart" in line:
+                path = line.split()[-1]
+                break
+        self.rt = ctypes.CDLL(path or "libcudart.so")
+        self.rt.cudaEventRecordWithFlags.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
+        self.rt.cudaEventRecordWithFlags.restype = ctypes.c_int
+
+    def record(self, ev: torch.cuda.Event, stream: torch.cuda.Stream):
+        r = self.rt.cudaEventRecordWithFlags(ctypes.c_void_p(ev.cuda_event), ctypes.c_void_p(stream.cuda_stream), 1)
+        if r != 0:
+            raise RuntimeError(f"cudaEventRecordWithFlags failed: {r}")
+
+
+# ----------------------------------------------------------------------------- algorithmic bytes
+def decode_bytes(w, step: int, C: int):
+    """Algorithmic HBM bytes of decode step `step` for all units: (attention, whole step).
+    Attention reads every attended K and V row once (bf16, 256 B each) for all
+    g heads, the indices, q, and writes out (fp32).  Scoring reads the bf16
+    centroid table and q, writes the scores; selection reads scores, sizes,
+    offsets and the selected perm entries, writes idx and count."""
+    U, g, d, B = w.units, w.g, w.d, w.B
+    pend = step % w.m + 1
+    rows = w.sinks + pend + B
+    attn = U * (rows * 2 * d * 2 + B * 4 + 4 + g * d * 2 + g * d * 4)
+    score = U * (C * d * 2 + g * d * 2 + C * 4)
+    select = U * (C * 4 + C * 4 + (C + 1) * 4 + B * 4 + B * 4 + 4)
+    return attn, attn + score + select
+
+
+def kmeans_flops_bytes(w):
+    """Per prefill clustering of all units: assignment FLOPs (2 n C d per
+    iteration) and the two key passes per iteration (assign + update)."""
+    n = w.L - w.sinks
+    flops = w.iters * w.units * 2.0 * n * w.C * w.d
+    byts = w.iters * w.units * (2 * n * w.d * 2 + n * 4 * 4)
+    return flops, byts
+
+
+# ----------------------------------------------------------------------------- our path
+def run_ours(args, w, rank, world, device):
+    from recallable_kv_cache_gb300 import ckv
+    torch.cuda.set_device(device)
+    if world > 1:  # weak scaling: every rank its own sequence batch
+        w = synth.scaled(w, seed=w.seed + 1000 * rank)
+    U, L, B, T = w.units, w.L, w.B, w.decode_steps
+    K, V = synth.make_kv(w, device="cuda")
+    Q = synth.make_queries(w, T, device="cuda")
+    torch.cuda.synchronize()
+    ctx = ckv.Context(units=U, g=w.g, max_len=w.max_len, max_clusters=w.max_clusters, max_budget=B,
+                      iters=w.iters, m=w.m, c_plus=w.c_plus)
+    idx = torch.empty(U, B, dtype=torch.int32, device="cuda")
+    cnt = torch.empty(U, dtype=torch.int32, device="cuda")
+    out = torch.empty(U, w.g, w.d, dtype=torch.float32, device="cuda")
+    ext = ExternalEvents()
+
+    # eager pass first (validates every call), then capture
+    ctx.cluster_prefill(K, L, w.C)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g_pre, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(T)]
+    for e3 in ev:  # torch creates the CUDA event on first record
+        for e in e3:
+            e.record(s)
+    s.synchronize()
+    launches = {"prefill": 1 + w.iters * 6, "decode": 3 * T + w.n_incremental}
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g_pre, stream=s):
+            ctx.cluster_prefill(K, L, w.C)
+        with torch.cuda.graph(g_dec, stream=s):
+            for t in range(T):
+                if t > 0 and t % w.m == 0:
+                    ctx.cluster_incremental(K, L + t - w.m)
+                q = Q[t]
+                ext.record(ev[t][0], s)
+                ctx.select(q, B, idx, cnt)
+                ext.record(ev[t][1], s)
+                ctx.sparse_decode_attn(q, K, V, idx, cnt, B, L + t + 1, out)
+                ext.record(ev[t][2], s)
+    C_at = [w.C + w.c_plus * (t // w.m) for t in range(T)]
+    p0, p1, p2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+
+    def one_step(sample):
+        with torch.cuda.stream(s):
+            p0.record(s)
+            g_pre.replay()
+            p1.record(s)
+            g_dec.replay()
+            p2.record(s)
+        torch.cuda.synchronize()
+        if sample is not None:
+            sample["prefill"].append(p0.elapsed_time(p1))
+            sample["decode"].append(p1.elapsed_time(p2))
+            sample["select"].append(sum(ev[t][0].elapsed_time(ev[t][1]) for t in range(T)))
+            sample["attn"].append(sum(ev[t][1].elapsed_time(ev[t][2]) for t in range(T)))
+
+    for _ in range(args.warmup):
+        one_step(None)
+    assert ctx.device_error() == 0
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    smi_index = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[device] if os.environ.get(
+        "CUDA_VISIBLE_DEVICES") else device
+    clk = ClockSampler(smi_index)
+    clk.start()
+    time.sleep(0.3)
+    sample = {"prefill": [], "decode": [], "select": [], "attn": []}
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for _ in range(args.steps):
+        one_step(sample)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = clk.stop()
+    err = ctx.device_error()
+    if err:
+        raise RuntimeError(f"device error {err} during the timed region")
+
+    step_ms = [a + b for a, b in zip(sample["prefill"], sample["decode"])]
+    res = dict(step_ms=sum(step_ms) / len(step_ms), prefill_ms=statistics.mean(sample["prefill"]),
+               decode_ms=statistics.mean(sample["decode"]), select_ms=statistics.mean(sample["select"]),
+               attn_ms=statistics.mean(sample["attn"]), wall_s=wall, clocks=clocks,
+               launches=(launches["prefill"] + launches["decode"]) * args.steps)
+    attn_b = sum(decode_bytes(w, t, C_at[t])[0] for t in range(T))
+    step_b = sum(decode_bytes(w, t, C_at[t])[1] for t in range(T))
+    res["attn_bytes_per_launch"] = attn_b / T
+    res["decode_bytes_per_step"] = step_b / T
+    res["w"] = w
+    res["ctx"] = ctx
+    res["tensors"] = (K, V, Q)
+    if not args.no_e2e:
+        res["e2e"] = run_e2e(ctx, w, K, V, Q)
+    return res
+
+
+def run_e2e(ctx, w, K, V, Q):
+    """The same job through the public API from pinned host buffers: upload the
+    prompt K/V, prefill clustering, then per decode step upload q and the new
+    K/V row of every unit, select, attend, and read the output back."""
+    U, L, B, T, d = w.units, w.L, w.B, w.decode_steps, w.d
+    Kh = torch.empty(U, w.max_len, d, dtype=K.dtype, pin_memory=True)
+    Vh = torch.empty_like(Kh, pin_memory=True)
+    Kh.copy_(K)
+    Vh.copy_(V)
+    Qh = torch.empty(Q.shape, dtype=Q.dtype, pin_memory=True)
+    Qh.copy_(Q)
+    knew = Kh[:, L:].transpose(0, 1).contiguous().pin_memory()   # [T, U, d]
+    vnew = Vh[:, L:].transpose(0, 1).contiguous().pin_memory()
+    outh = torch.empty(T, U, w.g, d, dtype=torch.float32, pin_memory=True)
+    Kd = torch.empty_like(K)
+    Vd = torch.empty_like(V)
+    qd = torch.empty(U, w.g, d, dtype=Q.dtype, device="cuda")
+    idx = torch.empty(U, B, dtype=torch.int32, device="cuda")
+    cnt = torch.empty(U, dtype=torch.int32, device="cuda")
+    out = torch.empty(U, w.g, d, dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+
+    def job():
+        for u in range(U):
+            Kd[u, :L].copy_(Kh[u, :L], non_blocking=True)
+            Vd[u, :L].copy_(Vh[u, :L], non_blocking=True)
+        ctx.cluster_prefill(Kd, L, w.C)
+        for t in range(T):
+            if t > 0 and t % w.m == 0:
+                ctx.cluster_incremental(Kd, L + t - w.m)
+            qd.copy_(Qh[t], non_blocking=True)
+            Kd[:, L + t].copy_(knew[t], non_blocking=True)
+            Vd[:, L + t].copy_(vnew[t], non_blocking=True)
+            ctx.select(qd, B, idx, cnt)
+            ctx.sparse_decode_attn(qd, Kd, Vd, idx, cnt, B, L + t + 1, out)
+            outh[t].copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+
+    job()  # warm-up
+    t0 = time.perf_counter()
+    job()
+    dt = time.perf_counter() - t0
+    h2d = 2 * U * L * d * 2 + T * (U * w.g * d * 2 + 2 * U * d * 2)
+    d2h = T * U * w.g * d * 4
+    return {"value": T / dt, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "job_s": dt}
+
+
+# ----------------------------------------------------------------------------- the oracle on the CPU
+def oracle_unit_job(w, K, V, Q):
+    """One unit's whole job on the CPU oracle: prefill clustering, then every
+    decode step (incremental clustering every m steps, score, select, sparse
+    attention).  Returns (prefill seconds, decode seconds)."""
+    import oracle.clusterkv as ck
+    t0 = time.perf_counter()
+    st = ck.cluster_prefill(K, w.L, w.C, iters=w.iters, operand="bf16")
+    t1 = time.perf_counter()
+    end = w.L
+    for t in range(w.decode_steps):
+        if t > 0 and t % w.m == 0:
+            inc = ck.cluster_incremental(K, end, w.m, w.c_plus, iters=w.iters, operand="bf16")
+            st = ck.append_clusters(st, inc)
+            end += w.m
+        q = Q[t]
+        idx, _ = ck.select(ck.score(q, st["mu"]), st["sizes"], st["offsets"], st["perm"], w.B)
+        ck.sparse_attention(q, K, V, ck.attention_tokens(w.sinks, end, w.L + t + 1, idx))
+    t2 = time.perf_counter()
+    return t1 - t0, t2 - t1
+
+
+def oracle_sample(w, budget_s, device_tensors=None):
+    """Time the oracle on whole-unit jobs until `budget_s` seconds are spent
+    (at least one unit); scale to the full workload (units are independent)."""
+    times = []
+    t_start = time.perf_counter()
+    u = 0
+    while u < w.units and (u == 0 or time.perf_counter() - t_start < budget_s):
+        if device_tensors is not None:
+            K, V, Q = device_tensors
+            Ku, Vu, Qu = (x.double().cpu().numpy() for x in (K[u], V[u], Q[:, u]))
+        else:
+            Kt, Vt = synth.make_kv(w, units=[u])
+            Qt = synth.make_queries(w, w.decode_steps, units=[u])
+            Ku, Vu, Qu = Kt[0].double().numpy(), Vt[0].double().numpy(), Qt[:, 0].double().numpy()
+        times.append(oracle_unit_job(w, Ku, Vu, Qu))
+        u += 1
+    pre = statistics.mean(t[0] for t in times)
+    dec = statistics.mean(t[1] for t in times)
+    job_s = (pre + dec) * w.units
+    return {"tokens_per_s": w.decode_steps / job_s, "prefill_s_per_unit": pre, "decode_s_per_unit": dec,
+            "units": len(times), "job_s": job_s}
+
+
+def cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
+        return int(n)
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------------------- main
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    w = synth.WORKLOADS[args.workload]
+    cfg = {"workload": f"{w.name}: {w.layers} layers x {w.kv_heads} KV heads x batch {w.batch} "
+                       f"({w.units} units), d={w.d}, GQA {w.g}, prompt L={w.L}, {w.decode_steps} decode "
+                       f"steps, B={w.B}, C={w.C} + {w.c_plus} every {w.m} steps, {w.iters} Lloyd iterations",
+           "units": w.units, "L": w.L, "decode_steps": w.decode_steps, "B": w.B, "C": w.C,
+           "l2": "inputs larger than L2: 4.4 GB of K/V and 268 MB of queries resident; every decode "
+                 "step gathers ~166 MB of scattered rows (L2 is 129 MB); no flush"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        steps = []
+        sample_desc = None
+        for i in range(args.warmup + args.steps):
+            r = oracle_sample(w, 0.0)
+            if i >= args.warmup:
+                steps.append(r)
+            sample_desc = (f"one unit's whole job per step (prefill clustering of {w.L - w.sinks} keys "
+                           f"+ {w.decode_steps} decode steps), scaled x{w.units} units")
+        v = statistics.mean(r["tokens_per_s"] for r in steps)
+        cores = cpu_threads()
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1000 * statistics.mean(r["job_s"] for r in steps),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": cfg,
+                "kmeans_ms_per_layer": 1000 * statistics.mean(r["prefill_s_per_unit"] for r in steps) * w.kv_heads * w.batch,
+                "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                 "sample": sample_desc},
+                "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    r = run_ours(args, w, rank, world, local)
+    w = r["w"]
+    hbm, peak_kind, meas = peaks()
+    step_ms, prefill_ms, decode_ms = r["step_ms"], r["prefill_ms"], r["decode_ms"]
+    if world > 1:
+        t = torch.tensor([step_ms, prefill_ms, decode_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_ms, prefill_ms, decode_ms = t.tolist()
+    T = w.decode_steps
+    value = world * T / (step_ms / 1000.0)
+    attn_gbs = r["attn_bytes_per_launch"] / (r["attn_ms"] / T / 1000.0) / 1e9
+    decode_gbs = r["decode_bytes_per_step"] / (decode_ms / T / 1000.0) / 1e9
+    kflops, kbytes = kmeans_flops_bytes(w)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
+        "decode_tokens_per_s": world * T / (decode_ms / 1000.0),
+        "kmeans_ms_per_layer": prefill_ms / w.layers / w.batch,
+        "decode_step_us": 1000.0 * decode_ms / T,
+        "decode_roofline": {"bound": "hbm", "achieved": decode_gbs, "peak": hbm, "unit": "GB/s",
+                            "frac": decode_gbs / hbm, "bytes_per_step": r["decode_bytes_per_step"],
+                            "peak_kind": peak_kind},
+        "kmeans_roofline": {"tflops": kflops / (prefill_ms / 1000.0) / 1e12,
+                            "peak_tflops": meas.get("bf16_tflops_sustained", 1700.0),
+                            "bytes_gbs": kbytes / (prefill_ms / 1000.0) / 1e9},
+        "roofline": {"bound": "hbm", "kernel": "attn_kernel (gather + split-K attention)",
+                     "achieved": attn_gbs, "peak": hbm, "unit": "GB/s", "frac": attn_gbs / hbm,
+                     "traffic": None, "bytes_per_launch": r["attn_bytes_per_launch"],
+                     "launch_us": 1000.0 * r["attn_ms"] / T, "peak_kind": peak_kind},
+        "phase_ms": {"prefill_clustering": prefill_ms, "decode_loop": decode_ms,
+                     "select_kernels": r["select_ms"], "attention_kernels": r["attn_ms"]},
+        "gpu_launches": r["launches"], "clocks": r["clocks"],
+    }
+    if "e2e" in r:
+        line["e2e"] = r["e2e"]
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = oracle_sample(w, args.cpu_seconds, r["tensors"])
+        line["cpu_baseline"] = {"value": cb["tokens_per_s"], "unit": "tokens/s", "cores": cpu_threads(),
+                                "kind": "oracle",
+                                "sample": f"{cb['units']} unit(s)' whole job (prefill clustering + "
+                                          f"{T} decode steps) on the host, scaled x{w.units} units"}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
