@@ -192,6 +192,37 @@ ckv_status ckv_sparse_decode_attn(ckv_ctx* ctx, const void* q, int32_t q_dtype, 
                                   const void* V, const int32_t* idx, const int32_t* count,
                                   int32_t B, int32_t cur_len, float* out, void* stream);
 
+/* Sparse decode attention that allocates nothing and needs no context.
+ * The ClusterKV paper has no counterpart of this call; it exists for callers
+ * that cannot allocate device memory: code running while a CUDA graph is
+ * being captured, engines whose memory planner owns the whole device, or
+ * processes that handed all free memory to a pooling allocator.  (Creating a
+ * ckv_ctx allocates, so those callers cannot use ckv_sparse_decode_attn.)
+ * It computes exactly what ckv_sparse_decode_attn computes, with the same
+ * kernel, for caller-given state: the attended set of unit u is tokens
+ * [0, sinks) + [clustered_end, cur_len) + idx[u][0..count[u]); q, K, V, idx,
+ * count and out have the layouts given at the top of this file (K and V with
+ * max_len rows per unit).  dev_err is an optional device int32 (NULL = none)
+ * that receives CKV_DEV_* codes.
+ * Scratch: the split partials and per-unit counters live in one fixed 8 MiB
+ * device array inside the library (held on every device that loads the
+ * library until the process exits).  A call needs
+ *   units * ceil((sinks + cur_len - clustered_end + B) / R) * g * 130 * 4
+ * bytes (rounded up to 256) + 4 * units bytes, with R = 64 rows for bf16 and
+ * g = 4 (see the kernel shape for other cases); larger calls return
+ * CKV_ERR_CAPACITY before launching anything.  The first call on each device
+ * looks the array's device address up (cudaGetSymbolAddress), so make that
+ * first call before any stream capture.  Every call reuses the same array
+ * (the counters are cleared on the stream at the start of each call), so
+ * calls that can overlap on the GPU (different streams without ordering)
+ * race and must not be issued.  Errors: CKV_ERR_ARG, CKV_ERR_DTYPE,
+ * CKV_ERR_ALIGN, CKV_ERR_CAPACITY, CKV_ERR_CUDA. */
+ckv_status ckv_sparse_decode_attn_noalloc(const void* q, int32_t q_dtype, const void* K,
+                                          const void* V, const int32_t* idx, const int32_t* count,
+                                          int32_t units, int32_t g, int32_t max_len, int32_t sinks,
+                                          int32_t clustered_end, int32_t cur_len, int32_t B,
+                                          float* out, int32_t* dev_err, void* stream);
+
 /* Host-side copy of the context's counters. */
 ckv_status ckv_get_info(ckv_ctx* ctx, ckv_info* info);
 

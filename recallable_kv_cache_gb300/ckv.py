@@ -36,6 +36,7 @@ SIGNATURES = {
     "ckv_export_clusters": ([_P, _P, _P, _P, _P, _P, _P], _I),
     "ckv_import_clusters": ([_P, _I, _I, _P, _P, _P, _P, _P], _I),
     "ckv_get_device_error": ([_P, ctypes.POINTER(_I)], _I),
+    "ckv_sparse_decode_attn_noalloc": ([_P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P], _I),
 }
 
 
@@ -191,3 +192,16 @@ class Context:
         v = ctypes.c_int32()
         _check(lib().ckv_get_device_error(self.handle, ctypes.byref(v)), "ckv_get_device_error")
         return v.value
+
+
+def sparse_decode_attn_noalloc(q, K, V, idx, count, units: int, g: int, max_len: int, sinks: int,
+                               clustered_end: int, cur_len: int, B: int, out, dev_err=None, stream=None):
+    """Sparse decode attention without a context and without any allocation:
+    for callers that may not allocate device memory (inside graph capture, or
+    under an engine that owns all device memory).  Its scratch is a fixed
+    8 MiB array inside the library; calls that overlap on the GPU race.  The
+    first call on a device must come before any stream capture."""
+    _check(lib().ckv_sparse_decode_attn_noalloc(ptr(q), _dtype_code(q), ptr(K), ptr(V), ptr(idx),
+                                                ptr(count), units, g, max_len, sinks, clustered_end,
+                                                cur_len, B, ptr(out), ptr(dev_err), _stream(stream)),
+           "ckv_sparse_decode_attn_noalloc")

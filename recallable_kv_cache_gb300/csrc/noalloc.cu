@@ -1,0 +1,84 @@
+// Sparse decode attention for callers that cannot allocate device memory.
+//
+// Some callers cannot call cudaMalloc at all: code that runs inside a CUDA
+// graph being captured, an engine whose memory planner owns every byte of the
+// device and forbids outside allocations, or a process that has handed all free
+// memory to a pooling allocator.  ckv_sparse_decode_attn needs a context, and
+// creating one allocates the split-K workspace.  This entry point runs the same
+// attention kernel without a context: its only scratch (the per-split partial
+// results and the per-unit arrival counters of the split combine) lives in one
+// fixed-size array in the library's own device memory, reserved when the
+// library is loaded and kept until the process exits.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "internal.h"
+
+namespace {
+
+constexpr size_t SCRATCH_BYTES = (size_t)8 << 20;  // 8 MiB per device that loads the library
+constexpr int MAX_DEVICES = 64;
+
+static __device__ __align__(256) unsigned char g_attn_scratch[SCRATCH_BYTES];
+
+std::mutex g_lock;
+void* g_scratch_addr[MAX_DEVICES];
+
+// Device address of the scratch array on the current device, looked up once
+// per device (the host-side symbol is only a stand-in, never a device address).
+cudaError_t scratch_address(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= MAX_DEVICES) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> guard(g_lock);
+    if (!g_scratch_addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_attn_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return cudaSuccess;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" ckv_status ckv_sparse_decode_attn_noalloc(const void* q, int32_t q_dtype, const void* K,
+                                                     const void* V, const int32_t* idx,
+                                                     const int32_t* count, int32_t units, int32_t g,
+                                                     int32_t max_len, int32_t sinks, int32_t clustered_end,
+                                                     int32_t cur_len, int32_t B, float* out,
+                                                     int32_t* dev_err, void* stream) {
+    using namespace ckv;
+    if (!q || !K || !V || !idx || !count || !out) return CKV_ERR_ARG;
+    if (q_dtype != CKV_F32 && q_dtype != CKV_BF16) return CKV_ERR_DTYPE;
+    if (g != 1 && g != 2 && g != 4 && g != 8) return CKV_ERR_ARG;
+    if (units < 1 || sinks < 0 || B < 0 || clustered_end < sinks || cur_len < clustered_end ||
+        cur_len > max_len)
+        return CKV_ERR_ARG;
+    if (!aligned16(q) || !aligned16(K) || !aligned16(V) || !aligned16(out)) return CKV_ERR_ALIGN;
+
+    const int rs = attention_rows_per_split(q_dtype, g);
+    const long long rows = (long long)sinks + (cur_len - clustered_end) + B;
+    const long long splits = (rows + rs - 1) / rs;
+    const long long part_bytes = (long long)units * splits * g * (D + 2) * (long long)sizeof(float);
+    const long long cnt_off = (part_bytes + 255) / 256 * 256;
+    const long long need = cnt_off + (long long)units * (long long)sizeof(int32_t);
+    if (need > (long long)SCRATCH_BYTES) return CKV_ERR_CAPACITY;
+
+    void* base = nullptr;
+    if (scratch_address(&base) != cudaSuccess) return CKV_ERR_CUDA;
+    float* part = static_cast<float*>(base);
+    int32_t* counters = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(base) + cnt_off);
+    cudaStream_t s = (cudaStream_t)stream;
+    // the split combine counts arrivals from zero; the previous call's contents remain
+    if (cudaMemsetAsync(counters, 0, (size_t)units * sizeof(int32_t), s) != cudaSuccess) return CKV_ERR_CUDA;
+    const cudaError_t e = launch_attention(q, K, V, idx, count, units, g, q_dtype, max_len, sinks, clustered_end,
+                                           cur_len, B, out, part, counters, (int)splits, dev_err, 0, s);
+    return e == cudaSuccess ? CKV_OK : CKV_ERR_CUDA;
+}
