@@ -47,6 +47,8 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget")
+    p.add_argument("--units", type=int, default=0, help="override the unit count (small profiling cases)")
+    p.add_argument("--decode-steps", type=int, default=0, help="override the decode steps (profiling)")
     return p.parse_args()
 
 
@@ -356,6 +358,10 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     w = synth.WORKLOADS[args.workload]
+    if args.units:
+        w = synth.scaled(w, units=args.units)
+    if args.decode_steps:
+        w = synth.scaled(w, decode_steps=args.decode_steps)
     cfg = {"workload": f"{w.name}: {w.layers} layers x {w.kv_heads} KV heads x batch {w.batch} "
                        f"({w.units} units), d={w.d}, GQA {w.g}, prompt L={w.L}, {w.decode_steps} decode "
                        f"steps, B={w.B}, C={w.C} + {w.c_plus} every {w.m} steps, {w.iters} Lloyd iterations",
@@ -408,7 +414,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
         "decode_tokens_per_s": world * T / (decode_ms / 1000.0),
-        "kmeans_ms_per_layer": prefill_ms / w.layers / w.batch,
+        "kmeans_ms_per_layer": prefill_ms * w.kv_heads / w.units,
         "decode_step_us": 1000.0 * decode_ms / T,
         "decode_roofline": {"bound": "hbm", "achieved": decode_gbs, "peak": hbm, "unit": "GB/s",
                             "frac": decode_gbs / hbm, "bytes_per_step": r["decode_bytes_per_step"],

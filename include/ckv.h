@@ -208,8 +208,9 @@ ckv_status ckv_sparse_decode_attn(ckv_ctx* ctx, const void* q, int32_t q_dtype, 
  * device array inside the library (held on every device that loads the
  * library until the process exits).  A call needs
  *   units * ceil((sinks + cur_len - clustered_end + B) / R) * g * 130 * 4
- * bytes (rounded up to 256) + 4 * units bytes, with R = 64 rows for bf16 and
- * g = 4 (see the kernel shape for other cases); larger calls return
+ * bytes (rounded up to 256) + 4 * units bytes, where R is the rows of one
+ * attention work item: 16 for bf16, 64 for fp32 with g <= 4 and 32 for fp32
+ * with g = 8; larger calls return
  * CKV_ERR_CAPACITY before launching anything.  The first call on each device
  * looks the array's device address up (cudaGetSymbolAddress), so make that
  * first call before any stream capture.  Every call reuses the same array

@@ -243,9 +243,10 @@ ckv_status ckv_select_scored(ckv_ctx* ctx, const float* scores, int32_t B, int32
     if (B < 0) return CKV_ERR_ARG;
     if (B > ctx->cfg.max_budget) return CKV_ERR_CAPACITY;
     if (ctx->n_clusters <= 0 || ctx->clustered_end <= ctx->cfg.sinks) return CKV_ERR_STATE;
+    if (ctx->n_clusters > MAX_SELECT_CLUSTERS) return CKV_ERR_UNIMPLEMENTED;
     cudaStream_t s = (cudaStream_t)stream;
     ctx->last_stream = s;
-    return cuda_status(launch_select(ctx, scores, ctx->n_clusters, ctx->n_clusters, B, idx, count, s));
+    return cuda_status(launch_select(ctx, nullptr, scores, ctx->n_clusters, ctx->n_clusters, B, idx, count, s));
 }
 
 ckv_status ckv_select(ckv_ctx* ctx, const void* q, int32_t q_dtype, int32_t B, int32_t* idx, int32_t* count,
@@ -256,11 +257,10 @@ ckv_status ckv_select(ckv_ctx* ctx, const void* q, int32_t q_dtype, int32_t B, i
     if (B < 0) return CKV_ERR_ARG;
     if (B > ctx->cfg.max_budget) return CKV_ERR_CAPACITY;
     if (ctx->n_clusters <= 0 || ctx->clustered_end <= ctx->cfg.sinks) return CKV_ERR_STATE;
+    if (ctx->n_clusters > MAX_SELECT_CLUSTERS) return CKV_ERR_UNIMPLEMENTED;
     cudaStream_t s = (cudaStream_t)stream;
     ctx->last_stream = s;
-    cudaError_t e = launch_score(ctx, q, ctx->n_clusters, ctx->scores, ctx->cmax, s);
-    if (e == cudaSuccess) e = launch_select(ctx, ctx->scores, ctx->cmax, ctx->n_clusters, B, idx, count, s);
-    return cuda_status(e);
+    return cuda_status(launch_select(ctx, q, nullptr, 0, ctx->n_clusters, B, idx, count, s));
 }
 
 ckv_status ckv_sparse_decode_attn(ckv_ctx* ctx, const void* q, int32_t q_dtype, const void* K, const void* V,

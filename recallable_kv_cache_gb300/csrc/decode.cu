@@ -110,90 +110,185 @@ __device__ __forceinline__ uint64_t rank_key(float s, int c) {
     return ((uint64_t)(~ord) << 32) | (uint32_t)c;                      // descending score, asc c
 }
 
-constexpr int SEL_THREADS = 512;
-
-__global__ void __launch_bounds__(SEL_THREADS) select_kernel(
-    const float* __restrict__ scores, int stride, int C, int npow2, const int32_t* __restrict__ sizes,
-    const int32_t* __restrict__ offsets, const int32_t* __restrict__ perm, int cmax, int ntok, int B,
-    int32_t* __restrict__ idx, int32_t* __restrict__ count, int32_t* __restrict__ dev_err) {
+// One CTA per unit.  Scores (computed here from q and the bf16 centroid copy,
+// or read from the caller) become 64-bit keys (descending score, ascending
+// cluster index) that are sorted by a bitonic network held in registers:
+// exchange distances below 32 use warp shuffles, larger ones shared memory,
+// and distances of at least the block size stay inside a thread (E keys per
+// thread).  The sizes taken in rank order are prefix-summed, the budget cut
+// found, and every output slot p < min(B, total) looks up its rank by binary
+// search and copies its token id from the label-sorted permutation.
+// All global reads except the permutation (q, centroid rows, sizes, offsets)
+// are issued before any of them is used, so they share one round trip.
+template <typename T, int G, int E, bool FROM_SCORES>
+__global__ void __launch_bounds__(1024, 1) sel_kernel(
+    const T* __restrict__ q, const T* __restrict__ mu, int cmax, const float* __restrict__ scores_in,
+    int sstride, int C, int N, const int32_t* __restrict__ sizes, const int32_t* __restrict__ offsets,
+    const int32_t* __restrict__ perm, int ntok, int B, int32_t* __restrict__ idx,
+    int32_t* __restrict__ count, int32_t* __restrict__ dev_err) {
     extern __shared__ __align__(16) unsigned char sel_smem[];
-    uint64_t* keys = reinterpret_cast<uint64_t*>(sel_smem);
-    int32_t* start = reinterpret_cast<int32_t*>(keys + npow2);
-    int32_t* rc = start + npow2;
-    __shared__ int32_t warp_tot[SEL_THREADS / 32];
-    __shared__ int32_t s_total;
+    uint64_t* sk = reinterpret_cast<uint64_t*>(sel_smem);  // [N]
+    int32_t* start = reinterpret_cast<int32_t*>(sk + N);   // [N]
+    int32_t* cl = start + N;                               // [N]
+    int32_t* szc = cl + N;                                 // [N] sizes by cluster
+    int32_t* offc = szc + N;                               // [N] offsets by cluster
+    __shared__ int32_t wsum[32];
+    __shared__ int32_t s_tot;
+    const int u = blockIdx.x, tid = threadIdx.x, NT = blockDim.x;
+    const int lane = tid & 31, warp = tid >> 5, nwarps = NT >> 5;
 
-    const int u = blockIdx.x;
-    const int tid = threadIdx.x;
-    const float* sc = scores + (size_t)u * stride;
-    for (int i = tid; i < npow2; i += SEL_THREADS) keys[i] = i < C ? rank_key(sc[i], i) : ~0ull;
+    // ---- 1. sizes / offsets (registers first, shared memory after the scores)
+    int szr[E], ofr[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        const int c = e * NT + tid;
+        szr[e] = c < C ? sizes[(size_t)u * cmax + c] : 0;
+        ofr[e] = c < C ? offsets[(size_t)u * (cmax + 1) + c] : 0;
+    }
+    // ---- 2. unsorted keys
+    if constexpr (FROM_SCORES) {
+        for (int c = tid; c < N; c += NT) sk[c] = c < C ? rank_key(scores_in[(size_t)u * sstride + c], c) : ~0ull;
+    } else {
+        constexpr int CPL = Vec<T>::N, LPR = D / CPL, RPI = 32 / LPR, UNR = 8;
+        const int sub = lane / LPR, li = lane % LPR;
+        const T* mu_u = mu + (size_t)u * cmax * D + li * CPL;
+        const int step = nwarps * RPI;
+        uint4 qw[G], v[UNR];
+#pragma unroll
+        for (int h = 0; h < G; ++h) qw[h] = *reinterpret_cast<const uint4*>(q + ((size_t)u * G + h) * D + li * CPL);
+        // rb is the same for every lane of the warp (the loop below holds
+        // full-warp shuffles); the row of a lane is rb + sub + i * step
+        int rb = warp * RPI;
+        auto load_rows = [&](int b) {
+#pragma unroll
+            for (int i = 0; i < UNR; ++i) {
+                const int r = b + sub + i * step;
+                v[i] = r < C ? *reinterpret_cast<const uint4*>(mu_u + (size_t)r * D) : make_uint4(0, 0, 0, 0);
+            }
+        };
+        load_rows(rb);
+        // sum of the g query heads for channels li*CPL .. +CPL
+        float qc[CPL];
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) qc[c] = 0.f;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            float f[CPL];
+            Vec<T>::unpack(qw[h], f);
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) qc[c] += f[c];
+        }
+        for (; rb < C; rb += step * UNR) {
+#pragma unroll
+            for (int i = 0; i < UNR; ++i) {
+                float f[CPL];
+                Vec<T>::unpack(v[i], f);
+                float dot = 0.f;
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) dot = fmaf(qc[c], f[c], dot);
+#pragma unroll
+                for (int o = LPR / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(FULL, dot, o);
+                const int r = rb + sub + i * step;
+                if (li == 0 && r < C) sk[r] = rank_key(dot, r);
+            }
+            if (rb + step * UNR < C) load_rows(rb + step * UNR);
+        }
+        for (int c = C + tid; c < N; c += NT) sk[c] = ~0ull;
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        szc[e * NT + tid] = szr[e];
+        offc[e * NT + tid] = ofr[e];
+    }
     __syncthreads();
 
-    // bitonic sort, ascending keys
-    for (int k = 2; k <= npow2; k <<= 1) {
+    // ---- 3. bitonic sort, ascending keys; position i = e * NT + tid
+    uint64_t kv[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) kv[e] = sk[e * NT + tid];
+    for (int k = 2; k <= N; k <<= 1) {
         for (int j = k >> 1; j > 0; j >>= 1) {
-            for (int i = tid; i < (npow2 >> 1); i += SEL_THREADS) {
-                const int lo = ((i & ~(j - 1)) << 1) | (i & (j - 1));
-                const int hi = lo + j;
-                const uint64_t a = keys[lo], b = keys[hi];
-                const bool up = (lo & k) == 0;
-                if ((a > b) == up) {
-                    keys[lo] = b;
-                    keys[hi] = a;
+            if (j >= NT) {
+                const int ej = j / NT;
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    if (e & ej) continue;
+                    const int pe = e | ej;
+                    const int i = e * NT + tid;
+                    const bool up = (i & k) == 0;
+                    const uint64_t x = kv[e], y = kv[pe];
+                    if ((x > y) == up) {
+                        kv[e] = y;
+                        kv[pe] = x;
+                    }
+                }
+            } else if (j >= 32) {
+                __syncthreads();
+#pragma unroll
+                for (int e = 0; e < E; ++e) sk[e * NT + tid] = kv[e];
+                __syncthreads();
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const int i = e * NT + tid;
+                    const uint64_t p = sk[i ^ j];
+                    const bool keep_min = ((i & j) == 0) == ((i & k) == 0);
+                    kv[e] = keep_min ? (kv[e] < p ? kv[e] : p) : (kv[e] < p ? p : kv[e]);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const int i = e * NT + tid;
+                    const uint64_t p = __shfl_xor_sync(FULL, kv[e], j);
+                    const bool keep_min = ((i & j) == 0) == ((i & k) == 0);
+                    kv[e] = keep_min ? (kv[e] < p ? kv[e] : p) : (kv[e] < p ? p : kv[e]);
                 }
             }
-            __syncthreads();
         }
     }
 
-    // sizes in rank order, exclusive prefix sum (each thread a contiguous run)
-    const int per = (npow2 + SEL_THREADS - 1) / SEL_THREADS;
-    const int r0 = tid * per;
-    int run = 0;
-    for (int r = r0; r < r0 + per && r < npow2; ++r) {
-        const int c = (int)(uint32_t)keys[r];
-        const int sz = r < C ? sizes[(size_t)u * cmax + c] : 0;
-        rc[r] = c;
-        start[r] = sz;  // temporarily the size
-        run += sz;
-    }
-    // block exclusive scan of the per-thread runs
-    const int lane = tid & 31, warp = tid >> 5;
-    int incl = run;
+    // ---- 4. sizes in rank order, exclusive prefix sum over positions
+    int base = 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(FULL, incl, o);
-        if (lane >= o) incl += t;
-    }
-    if (lane == 31) warp_tot[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        int wt = lane < SEL_THREADS / 32 ? warp_tot[lane] : 0;
-        int wi = wt;
+    for (int e = 0; e < E; ++e) {
+        const int i = e * NT + tid;
+        const int c = (int)(uint32_t)kv[e];
+        const int sz = i < C ? szc[c] : 0;
+        int incl = sz;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int t = __shfl_up_sync(FULL, wi, o);
-            if (lane >= o) wi += t;
+            const int t = __shfl_up_sync(FULL, incl, o);
+            if (lane >= o) incl += t;
         }
-        if (lane < SEL_THREADS / 32) warp_tot[lane] = wi - wt;  // exclusive
-        if (lane == 31) s_total = wi;
+        if (lane == 31) wsum[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            const int wt = lane < nwarps ? wsum[lane] : 0;
+            int wi = wt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(FULL, wi, o);
+                if (lane >= o) wi += t;
+            }
+            if (lane < nwarps) wsum[lane] = wi - wt;
+            if (lane == 31) s_tot = wi;  // the segment's total
+        }
+        __syncthreads();
+        const int seg_total = s_tot;
+        const int excl = base + wsum[warp] + incl - sz;
+        __syncthreads();
+        start[i] = excl;
+        cl[i] = i < C ? c : 0;
+        base += seg_total;
+        __syncthreads();
     }
-    __syncthreads();
-    int base = warp_tot[warp] + incl - run;
-    for (int r = r0; r < r0 + per && r < npow2; ++r) {
-        const int sz = start[r];
-        start[r] = base;
-        base += sz;
-    }
-    __syncthreads();
 
-    const int total = s_total;
+    // ---- 5. cut at the budget and compact the token ids
+    const int total = base;
     const int cnt = total < B ? total : B;
     if (tid == 0) count[u] = cnt;
-    const int32_t* off = offsets + (size_t)u * (cmax + 1);
     const int32_t* pu = perm + (size_t)u * ntok;
     int32_t* out = idx + (size_t)u * B;
-    for (int p = tid; p < cnt; p += SEL_THREADS) {
+    for (int p = tid; p < cnt; p += NT) {
         // largest rank r < C with start[r] <= p (that cluster is non-empty and holds p)
         int lo = 0, hi = C - 1;
         while (lo < hi) {
@@ -201,7 +296,7 @@ __global__ void __launch_bounds__(SEL_THREADS) select_kernel(
             if (start[mid] <= p) lo = mid;
             else hi = mid - 1;
         }
-        const int pos = off[rc[lo]] + (p - start[lo]);
+        const int pos = offc[cl[lo]] + (p - start[lo]);
         if ((unsigned)pos < (unsigned)ntok) {
             out[p] = pu[pos];
         } else {
@@ -241,305 +336,456 @@ __device__ __forceinline__ void xreduce(float (&a)[N], int li) {
 
 constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
 
+constexpr int ATT_CW = 8;                    // consumer warps per CTA
+constexpr int ATT_STAGES = 3;                // shared-memory ring depth
+constexpr int ATT_THREADS = 32 * (ATT_CW + 1);
+
 template <typename T, int G>
 struct AttnShape {
     static constexpr int CPL = Vec<T>::N;
     static constexpr int LPR = D / CPL;
     static constexpr int RPI = 32 / LPR;
-    // rows per lane group per block: enough values to fill the lanes (G*NB >= LPR)
-    static constexpr int NB = (LPR / G) > 8 ? (LPR / G) : 8;
+    // rows per lane group per block (fewer for 8 heads to bound registers); when
+    // G*NB < LPR the reduced logits end up replicated across lanes
+    static constexpr int NB = G >= 8 ? 4 : 8;
     static constexpr int NV = G * NB;              // partial dots per lane
     static constexpr int VPL = NV >= LPR ? NV / LPR : 1;
     static constexpr int LOGL = ilog2(LPR);
     static constexpr int H = ilog2(NV) < LOGL ? ilog2(NV) : LOGL;  // halving steps
     static constexpr int REPL = LOGL - H;          // replication bits
     static constexpr int GL = NB / VPL;            // value holders per head
-    static constexpr int RW = NB * RPI;            // rows per warp
-    static constexpr int RS = 4 * RW;              // rows per CTA (4 warps)
+    static constexpr int RB = NB * RPI;            // rows per consumer warp per stage
+    static constexpr int SR = ATT_CW * RB;         // rows per stage (one work item)
+    static constexpr int PW = G * (D + 2);         // floats of one softmax partial
+    static constexpr size_t SMEM = (size_t)ATT_STAGES * SR * D * sizeof(T) * 2   // K, V ring
+                                   + (size_t)ATT_CW * PW * sizeof(float)          // warp states
+                                   + (size_t)ATT_CW * RPI * NB * G * sizeof(float) // p exchange
+                                   + (size_t)ATT_STAGES * SR * sizeof(int32_t)    // token ids
+                                   + (size_t)ATT_STAGES * G * D * sizeof(T);      // q
 };
 
+struct AttnArgs {
+    const void* q;
+    const void* K;
+    const void* V;
+    const int32_t* idx;
+    const int32_t* count;
+    int max_len, sinks, clustered_end, cur_len, B;
+    int ipu;    // work items (stages of SR rows) per unit
+    int ipc;    // work items per CTA
+    int total;  // units * ipu
+    int max_slots;
+    float qscale;
+    float* out;
+    float* part;
+    int32_t* counters;
+    int32_t* dev_err;
+};
+
+// Persistent, warp-specialised sparse decode attention.  Work items are
+// (unit, SR consecutive rows of the unit's attended set: sinks, then pending
+// tokens, then the selected tokens); each CTA takes a contiguous range.
+//   warp 0 (producer): resolves the token ids of an item, then streams its K
+//     and V rows with 16-byte cp.async copies into one stage of a shared-memory
+//     ring, signalling an mbarrier; q of the unit rides along.
+//   warps 1..8 (consumers): RB rows each per item; logits of the g heads are
+//     reduced across the lanes of a row with a transposed shuffle reduction,
+//     an online softmax keeps (max, sum, acc) per head across all items of the
+//     same unit; at a unit boundary the warp states are merged (in a fixed
+//     order) into one partial per (unit, CTA).
+// attn_combine_kernel then merges the partials of each unit, in CTA order.
 template <typename T, int G>
-__global__ void __launch_bounds__(128) attn_kernel(
-    const T* __restrict__ q, const T* __restrict__ K, const T* __restrict__ V,
-    const int32_t* __restrict__ idx, const int32_t* __restrict__ count, int max_len, int sinks,
-    int clustered_end, int cur_len, int B, float qscale, float* __restrict__ out,
-    float* __restrict__ part, int32_t* __restrict__ counters, int32_t* __restrict__ dev_err) {
+__global__ void __launch_bounds__(ATT_THREADS, 1) attn_kernel(const AttnArgs a) {
     using S = AttnShape<T, G>;
-    constexpr int CPL = S::CPL, LPR = S::LPR, RPI = S::RPI, NB = S::NB, NV = S::NV,
-                  VPL = S::VPL, RW = S::RW, RS = S::RS;
-    constexpr int ROWB = D * (int)sizeof(T);
-    constexpr int PW = G * (D + 2);  // floats per partial
-
+    constexpr int CPL = S::CPL, LPR = S::LPR, RPI = S::RPI, NB = S::NB, NV = S::NV, VPL = S::VPL,
+                  RB = S::RB, SR = S::SR, PW = S::PW;
     extern __shared__ __align__(128) unsigned char attn_smem[];
-    T* Ks = reinterpret_cast<T*>(attn_smem);
-    T* Vs = Ks + RS * D;
-    float* red = reinterpret_cast<float*>(Vs + RS * D);  // [4 warps][PW]
-    float* ps = red + 4 * PW;                            // [4 warps][RPI][NB][G]
-    __shared__ __align__(8) uint64_t bars[4];
-    __shared__ int32_t toks[RS];
-    __shared__ int s_last;
+    T* sK = reinterpret_cast<T*>(attn_smem);                       // [STAGES][SR][D]
+    T* sV = sK + (size_t)ATT_STAGES * SR * D;                      // [STAGES][SR][D]
+    float* red = reinterpret_cast<float*>(sV + (size_t)ATT_STAGES * SR * D);  // [CW][PW]
+    float* psm = red + ATT_CW * PW;                                // [CW][RPI][NB][G]
+    int32_t* stok = reinterpret_cast<int32_t*>(psm + ATT_CW * RPI * NB * G);  // [STAGES][SR]
+    T* sq = reinterpret_cast<T*>(stok + ATT_STAGES * SR);          // [STAGES][G][D]
+    __shared__ int s_unit[ATT_STAGES], s_nrows[ATT_STAGES];
+    __shared__ __align__(8) uint64_t full[ATT_STAGES], empty[ATT_STAGES], red_full, red_free;
+    __shared__ int abort_flag;
 
-    const int u = blockIdx.y, s = blockIdx.x;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int pend = cur_len - clustered_end;
-    int cnt = count[u];
-    if (cnt < 0 || cnt > B) {
-        if (s == 0 && tid == 0) set_err(dev_err, CKV_DEV_BAD_COUNT);
-        cnt = cnt < 0 ? 0 : B;
-    }
-    const int R = sinks + pend + cnt;
-    const int nsplit = (R + RS - 1) / RS;
-    if (s >= nsplit) return;
-    const int r0 = s * RS;
-    const int nrows = min(RS, R - r0);
+    const int first = blockIdx.x * a.ipc;
+    const int nitems = min(a.total, first + a.ipc) - first;
+    const int pend = a.cur_len - a.clustered_end;
 
-    // ---- gather: lane l of warp w copies row w*RW + l
-    uint64_t* bar = &bars[warp];
-    int tok = -1;
-    const int myrow = warp * RW + lane;
-    if (lane < RW && myrow < nrows) {
-        const int r = r0 + myrow;
-        if (r < sinks) tok = r;
-        else if (r < sinks + pend) tok = clustered_end + (r - sinks);
-        else tok = idx[(size_t)u * B + (r - sinks - pend)];
-        if (tok < 0 || tok >= cur_len) {
-            set_err(dev_err, CKV_DEV_BAD_INDEX);
-            tok = -1;
+    if (tid == 0) {
+        for (int st = 0; st < ATT_STAGES; ++st) {
+            ptx::mbar_init(&full[st], 64);        // 32 header arrivals + 32 copy arrivals
+            ptx::mbar_init(&empty[st], ATT_CW);
         }
-        toks[myrow] = tok;
-    }
-    const unsigned vmask = __ballot_sync(FULL, tok >= 0);
-    const int nvalid = __popc(vmask);
-    if (lane == 0) {
-        ptx::mbar_init(bar, 1);
+        ptx::mbar_init(&red_full, ATT_CW);
+        ptx::mbar_init(&red_free, ATT_CW);
+        abort_flag = 0;
         ptx::fence_barrier_init();
     }
-    __syncwarp();
-    if (nvalid) {
-        if (lane == 0) ptx::mbar_arrive_expect_tx(bar, (uint32_t)nvalid * 2u * ROWB);
-        __syncwarp();
-        if (tok >= 0) {
-            const size_t off = ((size_t)u * max_len + tok) * D;
-            ptx::bulk_g2s(Ks + (size_t)myrow * D, K + off, ROWB, bar);
-            ptx::bulk_g2s(Vs + (size_t)myrow * D, V + off, ROWB, bar);
-        }
-    }
+    __syncthreads();
 
-    // ---- query (pre-scaled by log2(e)/sqrt(d)) while the copies fly
-    const int sub = lane / LPR, li = lane % LPR;
-    float qv[G][CPL];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-        const uint4 w = *reinterpret_cast<const uint4*>(q + ((size_t)u * G + h) * D + li * CPL);
-        float f[CPL];
-        Vec<T>::unpack(w, f);
-#pragma unroll
-        for (int c = 0; c < CPL; ++c) qv[h][c] = f[c] * qscale;
-    }
-    float acc[G][CPL];
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int c = 0; c < CPL; ++c) acc[h][c] = 0.f;
-    // m and the lane's share of l (of its own head)
-    float m[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) m[h] = -INFINITY;
-    float lsum = 0.f;
+    auto give_up = [&]() {
+        if (atomicExch(&abort_flag, 1) == 0) set_err(a.dev_err, CKV_DEV_TIMEOUT);
+    };
 
-    bool ok = true;
-    if (nvalid) ok = ptx::mbar_wait(bar, 0, WAIT_LIMIT, nullptr);
-    if (!ok) set_err(dev_err, CKV_DEV_TIMEOUT);
-    __syncwarp();
-
-    if (ok) {
-        // ---- logits for the NB rows of this lane group (rows wrow = j*RPI + sub)
-        float a[NV];
-#pragma unroll
-        for (int j = 0; j < NB; ++j) {
-            const int wrow = j * RPI + sub;
-            const uint4 w = *reinterpret_cast<const uint4*>(Ks + (size_t)(warp * RW + wrow) * D + li * CPL);
-            float f[CPL];
-            Vec<T>::unpack(w, f);
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                float d0 = 0.f;
-#pragma unroll
-                for (int c = 0; c < CPL; ++c) d0 = fmaf(qv[h][c], f[c], d0);
-                a[h * NB + j] = d0;
+    if (warp == 0) {
+        // ================================================================ producer
+        constexpr int LPC = D * (int)sizeof(T) / 16;  // lanes per row copy
+        constexpr int RPC = 32 / LPC;                 // rows per warp-wide copy
+        constexpr int EPC = 16 / (int)sizeof(T);      // elements per 16-byte chunk
+        const T* Kb = static_cast<const T*>(a.K);
+        const T* Vb = static_cast<const T*>(a.V);
+        const T* qb = static_cast<const T*>(a.q);
+        const int csub = lane / LPC, ch = lane % LPC;
+        int cur_u = -1, R = 0;
+        for (int it = 0; it < nitems; ++it) {
+            const int st = it % ATT_STAGES;
+            if (it >= ATT_STAGES &&
+                !__all_sync(FULL, ptx::mbar_wait(&empty[st], ((it / ATT_STAGES) - 1) & 1, WAIT_LIMIT, &abort_flag))) {
+                give_up();
+                break;
             }
+            const int item = first + it;
+            const int u = item / a.ipu, k = item % a.ipu;
+            if (u != cur_u) {
+                int cnt = a.count[u];
+                if (cnt < 0 || cnt > a.B) {
+                    if (lane == 0) set_err(a.dev_err, CKV_DEV_BAD_COUNT);
+                    cnt = cnt < 0 ? 0 : a.B;
+                }
+                R = a.sinks + pend + cnt;
+                cur_u = u;
+            }
+            const int row0 = k * SR;
+            const int nrows = max(0, min(SR, R - row0));
+            int32_t* tk = stok + st * SR;
+#pragma unroll
+            for (int qq = 0; qq < SR / 32; ++qq) {
+                const int rl = lane + 32 * qq;
+                int tok = -1;
+                if (rl < nrows) {
+                    const int r = row0 + rl;
+                    if (r < a.sinks) tok = r;
+                    else if (r < a.sinks + pend) tok = a.clustered_end + (r - a.sinks);
+                    else tok = a.idx[(size_t)u * a.B + (r - a.sinks - pend)];
+                    if (tok < 0 || tok >= a.cur_len) {
+                        set_err(a.dev_err, CKV_DEV_BAD_INDEX);
+                        tok = -1;
+                    }
+                }
+                tk[rl] = tok;
+            }
+            if (lane == 0) {
+                s_unit[st] = u;
+                s_nrows[st] = nrows;
+            }
+            __syncwarp();
+            // q of the unit (G rows of D elements)
+            for (int e = lane; e < G * D / EPC; e += 32)
+                ptx::cp_async16(sq + (size_t)st * G * D + e * EPC, qb + (size_t)u * G * D + e * EPC);
+            const size_t ubase = (size_t)u * a.max_len * D + ch * EPC;
+            T* dK = sK + (size_t)st * SR * D + ch * EPC;
+            T* dV = sV + (size_t)st * SR * D + ch * EPC;
+            for (int r = csub; r < nrows; r += RPC) {
+                const int tok = tk[r];
+                if (tok >= 0) {
+                    ptx::cp_async16(dK + (size_t)r * D, Kb + ubase + (size_t)tok * D);
+                    ptx::cp_async16(dV + (size_t)r * D, Vb + ubase + (size_t)tok * D);
+                }
+            }
+            ptx::mbar_arrive(&full[st]);           // header and ids written
+            ptx::cp_async_mbar_arrive(&full[st]);  // arrives when this lane's copies land
         }
-        xreduce<NV, LPR>(a, li);
-        // lane holds values v = b*VPL + t, b = li >> REPL; head = v / NB, row j = v % NB
+        ptx::cp_async_wait_all();
+    } else {
+        // ================================================================ consumers
+        const int w = warp - 1;
+        const int sub = lane / LPR, li = lane % LPR;
         const int b = li >> S::REPL;
         const int hl = (b * VPL) / NB;
-        float bm = -INFINITY;
-#pragma unroll
-        for (int t = 0; t < VPL; ++t) {
-            const int j = (b * VPL + t) % NB;
-            const int wrow = warp * RW + j * RPI + sub;
-            const bool valid = wrow < nrows && toks[wrow] >= 0;
-            if (!valid) a[t] = -INFINITY;
-            bm = fmaxf(bm, a[t]);
-        }
-        // max over the head's value holders (bits REPL .. REPL+log2(GL)-1 of li)
-#pragma unroll
-        for (int o = 1; o < S::GL; o <<= 1) bm = fmaxf(bm, __shfl_xor_sync(FULL, bm, o << S::REPL));
-        float mnew[G], scl[G];
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            const int src = (sub * LPR) + ((h * S::GL) << S::REPL);
-            const float hb = __shfl_sync(FULL, bm, src);
-            mnew[h] = fmaxf(m[h], hb);
-            scl[h] = (mnew[h] == -INFINITY) ? 1.f : exp2f(m[h] - mnew[h]);
-        }
-        float* pw = ps + warp * (RPI * NB * G) + sub * (NB * G);
-        float psum = 0.f;
-#pragma unroll
-        for (int t = 0; t < VPL; ++t) {
-            const int v = b * VPL + t;
-            const float p = (a[t] == -INFINITY) ? 0.f : exp2f(a[t] - mnew[hl]);
-            psum += p;
-            pw[(v % NB) * G + (v / NB)] = p;
-        }
-        lsum = lsum * scl[hl] + psum;
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            m[h] = mnew[h];
-#pragma unroll
-            for (int c = 0; c < CPL; ++c) acc[h][c] *= scl[h];
-        }
-        __syncwarp();
-        // ---- P V
-#pragma unroll
-        for (int j = 0; j < NB; ++j) {
-            const int wrow = j * RPI + sub;
-            const uint4 w = *reinterpret_cast<const uint4*>(Vs + (size_t)(warp * RW + wrow) * D + li * CPL);
-            float f[CPL];
-            Vec<T>::unpack(w, f);
-            float p[G];
-#pragma unroll
-            for (int h = 0; h < G; ++h) p[h] = pw[j * G + h];
-            const bool valid = (warp * RW + wrow) < nrows && toks[warp * RW + wrow] >= 0;
-            if (valid) {
-#pragma unroll
-                for (int h = 0; h < G; ++h)
-#pragma unroll
-                    for (int c = 0; c < CPL; ++c) acc[h][c] = fmaf(p[h], f[c], acc[h][c]);
-            }
-        }
-        // l of the lane's head: sum over the distinct value holders
-#pragma unroll
-        for (int o = 1; o < S::GL; o <<= 1) lsum += __shfl_xor_sync(FULL, lsum, o << S::REPL);
-    }
+        float* pw = psm + (size_t)w * (RPI * NB * G) + sub * (NB * G);
+        float qv[G][CPL], acc[G][CPL], m[G];
+        float lsum = 0.f;
+        int cur_u = -1, flushes = 0;
+        bool alive = true;
 
-    // ---- combine the RPI row groups of the warp (bf16: two half-warps)
-    float lh[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-        const int src = (sub * LPR) + ((h * S::GL) << S::REPL);
-        lh[h] = __shfl_sync(FULL, lsum, src);
-    }
-    if (RPI == 2) {
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            const float mo = __shfl_xor_sync(FULL, m[h], 16);
-            const float lo = __shfl_xor_sync(FULL, lh[h], 16);
-            const float M = fmaxf(m[h], mo);
-            const float fa = (M == -INFINITY) ? 0.f : exp2f(m[h] - M);
-            const float fb = (M == -INFINITY) ? 0.f : exp2f(mo - M);
-#pragma unroll
-            for (int c = 0; c < CPL; ++c) {
-                const float ao = __shfl_xor_sync(FULL, acc[h][c], 16);
-                acc[h][c] = acc[h][c] * fa + ao * fb;
-            }
-            lh[h] = lh[h] * fa + lo * fb;
-            m[h] = M;
-        }
-    }
-    float* rw = red + warp * PW;
-    if (sub == 0) {
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-#pragma unroll
-            for (int c = 0; c < CPL; ++c) rw[h * (D + 2) + li * CPL + c] = acc[h][c];
-        if (li == 0) {
+        auto reset = [&](int st) {
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-                rw[h * (D + 2) + D] = m[h];
-                rw[h * (D + 2) + D + 1] = lh[h];
+                const uint4 wq = *reinterpret_cast<const uint4*>(sq + (size_t)st * G * D + h * D + li * CPL);
+                float f[CPL];
+                Vec<T>::unpack(wq, f);
+                m[h] = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) {
+                    qv[h][c] = f[c] * a.qscale;
+                    acc[h][c] = 0.f;
+                }
             }
-        }
-    }
-    __syncthreads();
+            lsum = 0.f;
+        };
 
-    // ---- combine the 4 warps and write this split's partial
-    float* pp = part + ((size_t)u * gridDim.x + s) * PW;
-    for (int e = tid; e < G * D; e += 128) {
-        const int h = e / D, c = e % D;
-        float M = -INFINITY;
+        // merge the warp states of unit u into this CTA's partial for u: every
+        // consumer warp publishes its state, then combines 1/CW of the outputs
+        // over all warps in a fixed order
+        auto flush = [&](int u) -> bool {
+            float ls = lsum;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) M = fmaxf(M, red[w * PW + h * (D + 2) + D]);
-        float o = 0.f, l = 0.f;
+            for (int o = 1; o < S::GL; o <<= 1) ls += __shfl_xor_sync(FULL, ls, o << S::REPL);
+            float lh[G], mm[G], ac[G][CPL];
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            const float mw = red[w * PW + h * (D + 2) + D];
-            const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
-            o += red[w * PW + h * (D + 2) + c] * f;
-            l += red[w * PW + h * (D + 2) + D + 1] * f;
-        }
-        pp[h * (D + 2) + c] = o;
-        if (c == 0) {
-            pp[h * (D + 2) + D] = M;
-            pp[h * (D + 2) + D + 1] = l;
-        }
-    }
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-        const int prev = atomicAdd(&counters[u], 1);
-        s_last = (prev == nsplit - 1);
-    }
-    __syncthreads();
-    if (!s_last) return;
+            for (int h = 0; h < G; ++h) {
+                lh[h] = __shfl_sync(FULL, ls, (sub * LPR) + ((h * S::GL) << S::REPL));
+                mm[h] = m[h];
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) ac[h][c] = acc[h][c];
+            }
+            if constexpr (RPI == 2) {
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    const float mo = __shfl_xor_sync(FULL, mm[h], 16);
+                    const float lo = __shfl_xor_sync(FULL, lh[h], 16);
+                    const float M = fmaxf(mm[h], mo);
+                    const float fa = (M == -INFINITY) ? 0.f : exp2f(mm[h] - M);
+                    const float fb = (M == -INFINITY) ? 0.f : exp2f(mo - M);
+#pragma unroll
+                    for (int c = 0; c < CPL; ++c) {
+                        const float ao = __shfl_xor_sync(FULL, ac[h][c], 16);
+                        ac[h][c] = ac[h][c] * fa + ao * fb;
+                    }
+                    lh[h] = lh[h] * fa + lo * fb;
+                    mm[h] = M;
+                }
+            }
+            // the previous merge has finished reading the exchange area
+            if (flushes > 0 &&
+                !__all_sync(FULL, ptx::mbar_wait(&red_free, (flushes - 1) & 1, WAIT_LIMIT, &abort_flag)))
+                return false;
+            float* rw = red + (size_t)w * PW;
+            if (sub == 0) {
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+#pragma unroll
+                    for (int c = 0; c < CPL; ++c) rw[h * (D + 2) + li * CPL + c] = ac[h][c];
+                    if (li == 0) {
+                        rw[h * (D + 2) + D] = mm[h];
+                        rw[h * (D + 2) + D + 1] = lh[h];
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&red_full);
+            if (!__all_sync(FULL, ptx::mbar_wait(&red_full, flushes & 1, WAIT_LIMIT, &abort_flag)))
+                return false;
+            const int c0 = (u * a.ipu) / a.ipc;
+            float* pp = a.part + ((size_t)u * a.max_slots + (blockIdx.x - c0)) * PW;
+            for (int e = w * 32 + lane; e < G * D; e += ATT_CW * 32) {
+                const int h = e / D, c = e % D;
+                float M = -INFINITY;
+#pragma unroll
+                for (int ww = 0; ww < ATT_CW; ++ww) M = fmaxf(M, red[ww * PW + h * (D + 2) + D]);
+                float o = 0.f, l = 0.f;
+#pragma unroll
+                for (int ww = 0; ww < ATT_CW; ++ww) {
+                    const float mw = red[ww * PW + h * (D + 2) + D];
+                    const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+                    o += red[ww * PW + h * (D + 2) + c] * f;
+                    l += red[ww * PW + h * (D + 2) + D + 1] * f;
+                }
+                pp[h * (D + 2) + c] = o;
+                if (c == 0) {
+                    pp[h * (D + 2) + D] = M;
+                    pp[h * (D + 2) + D + 1] = l;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&red_free);
+            ++flushes;
+            return true;
+        };
 
-    // ---- last CTA of the unit: combine the splits in split order
-    __threadfence();
-    const float* pu = part + (size_t)u * gridDim.x * PW;
-    for (int e = tid; e < G * D; e += 128) {
-        const int h = e / D, c = e % D;
+        for (int it = 0; it < nitems && alive; ++it) {
+            const int st = it % ATT_STAGES;
+            if (!__all_sync(FULL, ptx::mbar_wait(&full[st], (it / ATT_STAGES) & 1, WAIT_LIMIT, &abort_flag))) {
+                give_up();
+                alive = false;
+                break;
+            }
+            const int u = s_unit[st], nrows = s_nrows[st];
+            if (u != cur_u) {
+                if (cur_u >= 0 && !flush(cur_u)) {
+                    give_up();
+                    alive = false;
+                    break;
+                }
+                cur_u = u;
+                reset(st);
+            }
+            const int wrow0 = w * RB;
+            if (wrow0 < nrows) {
+                const T* kb = sK + ((size_t)st * SR + wrow0) * D + li * CPL;
+                const T* vb = sV + ((size_t)st * SR + wrow0) * D + li * CPL;
+                const int32_t* tk = stok + st * SR + wrow0;
+                unsigned vbits = 0;
+#pragma unroll
+                for (int j = 0; j < NB; ++j) {
+                    const int r = j * RPI + sub;
+                    if (wrow0 + r < nrows && tk[r] >= 0) vbits |= 1u << j;
+                }
+                float av[NV];
+#pragma unroll
+                for (int j = 0; j < NB; ++j) {
+                    const uint4 wk = *reinterpret_cast<const uint4*>(kb + (size_t)(j * RPI + sub) * D);
+                    float f[CPL];
+                    Vec<T>::unpack(wk, f);
+#pragma unroll
+                    for (int h = 0; h < G; ++h) {
+                        float d0 = 0.f;
+#pragma unroll
+                        for (int c = 0; c < CPL; ++c) d0 = fmaf(qv[h][c], f[c], d0);
+                        av[h * NB + j] = d0;
+                    }
+                }
+                xreduce<NV, LPR>(av, li);
+                float bm = -INFINITY;
+#pragma unroll
+                for (int t = 0; t < VPL; ++t) {
+                    const int j = (b * VPL + t) % NB;
+                    if (!((vbits >> j) & 1u)) av[t] = -INFINITY;
+                    bm = fmaxf(bm, av[t]);
+                }
+#pragma unroll
+                for (int o = 1; o < S::GL; o <<= 1) bm = fmaxf(bm, __shfl_xor_sync(FULL, bm, o << S::REPL));
+                float mnew[G], scl[G];
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    const float hb = __shfl_sync(FULL, bm, (sub * LPR) + ((h * S::GL) << S::REPL));
+                    mnew[h] = fmaxf(m[h], hb);
+                    scl[h] = (mnew[h] == -INFINITY) ? 1.f : exp2f(m[h] - mnew[h]);
+                }
+                float mh = mnew[0], sh = scl[0];
+#pragma unroll
+                for (int h = 1; h < G; ++h)
+                    if (h == hl) {
+                        mh = mnew[h];
+                        sh = scl[h];
+                    }
+                float psum = 0.f;
+#pragma unroll
+                for (int t = 0; t < VPL; ++t) {
+                    const int v = b * VPL + t;
+                    const float p = (av[t] == -INFINITY) ? 0.f : exp2f(av[t] - mh);
+                    psum += p;
+                    pw[(v % NB) * G + (v / NB)] = p;
+                }
+                lsum = lsum * sh + psum;
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    m[h] = mnew[h];
+#pragma unroll
+                    for (int c = 0; c < CPL; ++c) acc[h][c] *= scl[h];
+                }
+                __syncwarp();
+#pragma unroll
+                for (int j = 0; j < NB; ++j) {
+                    if (!((vbits >> j) & 1u)) continue;
+                    const uint4 wv = *reinterpret_cast<const uint4*>(vb + (size_t)(j * RPI + sub) * D);
+                    float f[CPL];
+                    Vec<T>::unpack(wv, f);
+                    float p[G];
+#pragma unroll
+                    for (int h = 0; h < G; ++h) p[h] = pw[j * G + h];
+#pragma unroll
+                    for (int h = 0; h < G; ++h)
+#pragma unroll
+                        for (int c = 0; c < CPL; ++c) acc[h][c] = fmaf(p[h], f[c], acc[h][c]);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&empty[st]);
+        }
+        if (alive && cur_u >= 0 && !flush(cur_u)) give_up();
+    }
+}
+
+// One CTA per unit: merge the per-CTA softmax partials of the unit (slot
+// order) into o_h = acc / l.  The slots a unit has are fixed by the static
+// work split: CTAs (u*ipu)/ipc .. (u*ipu + ipu - 1)/ipc.
+template <int G>
+__global__ void __launch_bounds__(128) attn_combine_kernel(const float* __restrict__ part, int ipu, int ipc,
+                                                           int max_slots, float* __restrict__ out) {
+    constexpr int PW = G * (D + 2);
+    __shared__ float fs[16][G];
+    __shared__ float ls[G];
+    const int u = blockIdx.x, tid = threadIdx.x;
+    const int c0 = (u * ipu) / ipc, c1 = (u * ipu + ipu - 1) / ipc;
+    const int ncov = min(c1 - c0 + 1, 16);
+    const float* pu = part + (size_t)u * max_slots * PW;
+    if (tid < G) {
+        const int h = tid;
         float M = -INFINITY;
-        for (int t = 0; t < nsplit; ++t) M = fmaxf(M, __ldcg(pu + (size_t)t * PW + h * (D + 2) + D));
-        float o = 0.f, l = 0.f;
-        for (int t = 0; t < nsplit; ++t) {
-            const float mt = __ldcg(pu + (size_t)t * PW + h * (D + 2) + D);
+        for (int t = 0; t < ncov; ++t) M = fmaxf(M, pu[(size_t)t * PW + h * (D + 2) + D]);
+        float l = 0.f;
+        for (int t = 0; t < ncov; ++t) {
+            const float mt = pu[(size_t)t * PW + h * (D + 2) + D];
             const float f = (mt == -INFINITY) ? 0.f : exp2f(mt - M);
-            o += __ldcg(pu + (size_t)t * PW + h * (D + 2) + c) * f;
-            l += __ldcg(pu + (size_t)t * PW + h * (D + 2) + D + 1) * f;
+            fs[t][h] = f;
+            l += pu[(size_t)t * PW + h * (D + 2) + D + 1] * f;
         }
-        out[((size_t)u * G + h) * D + c] = l > 0.f ? o / l : 0.f;
+        ls[h] = l;
     }
-    if (tid == 0) counters[u] = 0;
+    __syncthreads();
+    for (int e = tid; e < G * D; e += 128) {
+        const int h = e / D, c = e % D;
+        float o = 0.f;
+        for (int t = 0; t < ncov; ++t) o += pu[(size_t)t * PW + h * (D + 2) + c] * fs[t][h];
+        out[((size_t)u * G + h) * D + c] = ls[h] > 0.f ? o / ls[h] : 0.f;
+    }
 }
 
 template <typename T, int G>
 cudaError_t launch_attn_t(const void* q, const void* K, const void* V, const int32_t* idx,
                           const int32_t* count, int units, int max_len, int sinks,
                           int clustered_end, int cur_len, int B, float* out, float* part,
-                          int32_t* counters, int max_splits, int32_t* dev_err, cudaStream_t st) {
+                          int32_t* counters, int max_splits, int32_t* dev_err, int num_sms,
+                          cudaStream_t st) {
     using S = AttnShape<T, G>;
-    const int rows = sinks + (cur_len - clustered_end) + B;
-    const int splits = (rows + S::RS - 1) / S::RS;
-    if (splits > max_splits) return cudaErrorInvalidValue;
-    const size_t smem = (size_t)2 * S::RS * D * sizeof(T) + (size_t)4 * G * (D + 2) * sizeof(float) +
-                        (size_t)4 * S::RPI * S::NB * G * sizeof(float);
+    AttnArgs a;
+    a.q = q;
+    a.K = K;
+    a.V = V;
+    a.idx = idx;
+    a.count = count;
+    a.max_len = max_len;
+    a.sinks = sinks;
+    a.clustered_end = clustered_end;
+    a.cur_len = cur_len;
+    a.B = B;
+    a.ipu = (sinks + (cur_len - clustered_end) + B + S::SR - 1) / S::SR;
+    if (a.ipu < 1) a.ipu = 1;
+    if (a.ipu > max_splits) return cudaErrorInvalidValue;
+    a.total = a.ipu * units;
+    int grid = num_sms > 0 ? num_sms : 148;
+    if (grid > a.total) grid = a.total;
+    a.ipc = (a.total + grid - 1) / grid;
+    // a unit spans at most 16 CTAs (the combine kernel's limit)
+    if (a.ipc * 15 < a.ipu) a.ipc = (a.ipu + 14) / 15;
+    grid = (a.total + a.ipc - 1) / a.ipc;
+    a.max_slots = max_splits;
+    a.qscale = 1.4426950408889634f / sqrtf((float)D);
+    a.out = out;
+    a.part = part;
+    a.counters = counters;
+    a.dev_err = dev_err;
     auto kern = attn_kernel<T, G>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::SMEM);
     if (e != cudaSuccess) return e;
-    const float qscale = 1.4426950408889634f / sqrtf((float)D);
-    dim3 grid(splits, units);
-    kern<<<grid, 128, smem, st>>>((const T*)q, (const T*)K, (const T*)V, idx, count, max_len, sinks,
-                                  clustered_end, cur_len, B, qscale, out, part, counters, dev_err);
+    kern<<<grid, ATT_THREADS, S::SMEM, st>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    attn_combine_kernel<G><<<units, 128, 0, st>>>(part, a.ipu, a.ipc, max_splits, out);
     return cudaGetLastError();
 }
 
@@ -570,35 +816,61 @@ cudaError_t launch_score(const ckv_ctx* ctx, const void* q, int C, float* scores
                                  stride, s);
 }
 
-cudaError_t launch_select(const ckv_ctx* ctx, const float* scores, int stride, int C, int B,
-                          int32_t* idx, int32_t* count, cudaStream_t s) {
-    int npow2 = 1;
-    while (npow2 < C) npow2 <<= 1;
-    if (npow2 < 2) npow2 = 2;
-    const size_t smem = (size_t)npow2 * 16;
-    cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+template <typename T, int G, int E, bool FS>
+cudaError_t launch_sel_t(const ckv_ctx* ctx, const void* q, const float* scores, int stride, int C, int N,
+                         int B, int32_t* idx, int32_t* count, cudaStream_t s) {
+    const size_t smem = (size_t)N * 24;
+    auto kern = sel_kernel<T, G, E, FS>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    select_kernel<<<ctx->cfg.units, SEL_THREADS, smem, s>>>(scores, stride, C, npow2, ctx->sizes,
-                                                            ctx->offsets, ctx->perm, ctx->cmax,
-                                                            ctx->ntok, B, idx, count, ctx->dev_err);
+    kern<<<ctx->cfg.units, N / E, smem, s>>>((const T*)q, (const T*)ctx->mu_s, ctx->cmax, scores, stride, C, N,
+                                             ctx->sizes, ctx->offsets, ctx->perm, ctx->ntok, B, idx, count,
+                                             ctx->dev_err);
     return cudaGetLastError();
+}
+
+template <typename T, int E, bool FS>
+cudaError_t launch_sel_g(const ckv_ctx* ctx, const void* q, const float* scores, int stride, int C, int N, int B,
+                         int32_t* idx, int32_t* count, cudaStream_t s) {
+    switch (ctx->cfg.g) {
+        case 1: return launch_sel_t<T, 1, E, FS>(ctx, q, scores, stride, C, N, B, idx, count, s);
+        case 2: return launch_sel_t<T, 2, E, FS>(ctx, q, scores, stride, C, N, B, idx, count, s);
+        case 4: return launch_sel_t<T, 4, E, FS>(ctx, q, scores, stride, C, N, B, idx, count, s);
+        case 8: return launch_sel_t<T, 8, E, FS>(ctx, q, scores, stride, C, N, B, idx, count, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <typename T, bool FS>
+cudaError_t launch_sel_e(const ckv_ctx* ctx, const void* q, const float* scores, int stride, int C, int B,
+                         int32_t* idx, int32_t* count, cudaStream_t s) {
+    int N = 128;
+    while (N < C) N <<= 1;
+    if (N <= 1024) return launch_sel_g<T, 1, FS>(ctx, q, scores, stride, C, N, B, idx, count, s);
+    if (N == 2048) return launch_sel_g<T, 2, FS>(ctx, q, scores, stride, C, N, B, idx, count, s);
+    if (N == 4096) return launch_sel_g<T, 4, FS>(ctx, q, scores, stride, C, N, B, idx, count, s);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_select(const ckv_ctx* ctx, const void* q, const float* scores, int stride, int C, int B,
+                          int32_t* idx, int32_t* count, cudaStream_t s) {
+    const bool bf16 = ctx->cfg.kv_dtype == CKV_BF16;
+    if (scores)
+        return bf16 ? launch_sel_e<__nv_bfloat16, true>(ctx, nullptr, scores, stride, C, B, idx, count, s)
+                    : launch_sel_e<float, true>(ctx, nullptr, scores, stride, C, B, idx, count, s);
+    return bf16 ? launch_sel_e<__nv_bfloat16, false>(ctx, q, nullptr, 0, C, B, idx, count, s)
+                : launch_sel_e<float, false>(ctx, q, nullptr, 0, C, B, idx, count, s);
 }
 
 int attention_rows_per_split(int kv_dtype, int g) {
     if (kv_dtype == CKV_BF16) {
-        switch (g) {
-            case 1: return AttnShape<__nv_bfloat16, 1>::RS;
-            case 2: return AttnShape<__nv_bfloat16, 2>::RS;
-            case 4: return AttnShape<__nv_bfloat16, 4>::RS;
-            case 8: return AttnShape<__nv_bfloat16, 8>::RS;
-        }
+        return attention_mma_rows_per_tile();
     } else {
         switch (g) {
-            case 1: return AttnShape<float, 1>::RS;
-            case 2: return AttnShape<float, 2>::RS;
-            case 4: return AttnShape<float, 4>::RS;
-            case 8: return AttnShape<float, 8>::RS;
+            case 1: return AttnShape<float, 1>::SR;
+            case 2: return AttnShape<float, 2>::SR;
+            case 4: return AttnShape<float, 4>::SR;
+            case 8: return AttnShape<float, 8>::SR;
         }
     }
     return 0;
@@ -609,17 +881,13 @@ cudaError_t launch_attention(const void* q, const void* K, const void* V, const 
                              int sinks, int clustered_end, int cur_len, int B, float* out,
                              float* part, int32_t* counters, int max_splits, int32_t* dev_err,
                              int num_sms, cudaStream_t s) {
-    (void)num_sms;
 #define CKV_ATTN(T, G)                                                                          \
     return launch_attn_t<T, G>(q, K, V, idx, count, units, max_len, sinks, clustered_end,      \
-                               cur_len, B, out, part, counters, max_splits, dev_err, s)
+                               cur_len, B, out, part, counters, max_splits, dev_err, num_sms, s)
     if (kv_dtype == CKV_BF16) {
-        switch (g) {
-            case 1: CKV_ATTN(__nv_bfloat16, 1);
-            case 2: CKV_ATTN(__nv_bfloat16, 2);
-            case 4: CKV_ATTN(__nv_bfloat16, 4);
-            case 8: CKV_ATTN(__nv_bfloat16, 8);
-        }
+        // bf16 K/V: tensor-core kernel (attn_mma.cu); fp32 K/V: CUDA-core kernel below
+        return launch_attention_mma(q, K, V, idx, count, units, g, max_len, sinks, clustered_end, cur_len, B,
+                                    out, part, max_splits, dev_err, num_sms, s);
     } else {
         switch (g) {
             case 1: CKV_ATTN(float, 1);

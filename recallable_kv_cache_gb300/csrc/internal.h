@@ -75,15 +75,24 @@ cudaError_t launch_incremental(const ckv_ctx* ctx, const void* K, int start, int
 // scores[u][c] = sum_h q_h . mu_c, written with row stride `stride`
 cudaError_t launch_score(const ckv_ctx* ctx, const void* q, int C, float* scores, int stride,
                          cudaStream_t s);
-cudaError_t launch_select(const ckv_ctx* ctx, const float* scores, int stride, int C, int B,
+// selection for every unit: scores from q and the centroids (scores == null)
+// or from caller-given scores [units][stride]
+cudaError_t launch_select(const ckv_ctx* ctx, const void* q, const float* scores, int stride, int C, int B,
                           int32_t* idx, int32_t* count, cudaStream_t s);
+constexpr int MAX_SELECT_CLUSTERS = 4096;
 // split-K sparse decode attention; partials/counters are caller-provided scratch
 cudaError_t launch_attention(const void* q, const void* K, const void* V, const int32_t* idx,
                              const int32_t* count, int units, int g, int kv_dtype, int max_len,
                              int sinks, int clustered_end, int cur_len, int B, float* out,
                              float* part, int32_t* counters, int max_splits, int32_t* dev_err,
                              int num_sms, cudaStream_t s);
-// rows of the attended set one attention CTA covers
+// rows of the attended set one attention work item covers (partials per unit
+// are bounded by ceil(rows / this))
 int attention_rows_per_split(int kv_dtype, int g);
+int attention_mma_rows_per_tile();
+cudaError_t launch_attention_mma(const void* q, const void* K, const void* V, const int32_t* idx,
+                                 const int32_t* count, int units, int g, int max_len, int sinks, int clustered_end,
+                                 int cur_len, int B, float* out, float* part, int max_slots, int32_t* dev_err,
+                                 int num_sms, cudaStream_t s);
 
 }  // namespace ckv

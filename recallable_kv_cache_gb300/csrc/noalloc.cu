@@ -25,10 +25,12 @@ static __device__ __align__(256) unsigned char g_attn_scratch[SCRATCH_BYTES];
 
 std::mutex g_lock;
 void* g_scratch_addr[MAX_DEVICES];
+int g_num_sms[MAX_DEVICES];
 
-// Device address of the scratch array on the current device, looked up once
-// per device (the host-side symbol is only a stand-in, never a device address).
-cudaError_t scratch_address(void** out) {
+// Device address of the scratch array on the current device (and the device's
+// SM count), looked up once per device: the host-side symbol is only a
+// stand-in, never a device address.
+cudaError_t scratch_address(void** out, int* num_sms) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -38,9 +40,14 @@ cudaError_t scratch_address(void** out) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_attn_scratch);
         if (e != cudaSuccess) return e;
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        g_num_sms[dev] = sms;
         g_scratch_addr[dev] = p;
     }
     *out = g_scratch_addr[dev];
+    *num_sms = g_num_sms[dev];
     return cudaSuccess;
 }
 
@@ -72,13 +79,14 @@ extern "C" ckv_status ckv_sparse_decode_attn_noalloc(const void* q, int32_t q_dt
     if (need > (long long)SCRATCH_BYTES) return CKV_ERR_CAPACITY;
 
     void* base = nullptr;
-    if (scratch_address(&base) != cudaSuccess) return CKV_ERR_CUDA;
+    int num_sms = 0;
+    if (scratch_address(&base, &num_sms) != cudaSuccess) return CKV_ERR_CUDA;
     float* part = static_cast<float*>(base);
     int32_t* counters = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(base) + cnt_off);
     cudaStream_t s = (cudaStream_t)stream;
     // the split combine counts arrivals from zero; the previous call's contents remain
     if (cudaMemsetAsync(counters, 0, (size_t)units * sizeof(int32_t), s) != cudaSuccess) return CKV_ERR_CUDA;
     const cudaError_t e = launch_attention(q, K, V, idx, count, units, g, q_dtype, max_len, sinks, clustered_end,
-                                           cur_len, B, out, part, counters, (int)splits, dev_err, 0, s);
+                                           cur_len, B, out, part, counters, (int)splits, dev_err, num_sms, s);
     return e == cudaSuccess ? CKV_OK : CKV_ERR_CUDA;
 }

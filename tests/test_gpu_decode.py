@@ -177,3 +177,48 @@ def test_select_ties_and_empty_clusters():
             assert cnt[u].item() == wc
             assert np.array_equal(idx[u, :wc].cpu().numpy(), want)
     ctx.close()
+
+
+@pytest.mark.parametrize("C", [129, 1500, 3000])
+def test_select_large_cluster_counts(C):
+    """Random CSR with many clusters (the sort then holds 1, 2 or 4 keys per
+    thread), tied scores, empty clusters: selection from given scores against
+    the oracle, and the fused path against scoring followed by selection."""
+    torch.cuda.init()
+    U, d = 2, 128
+    rng = np.random.default_rng(C)
+    n = 6 * C
+    L = 16 + n
+    ctx = make_ctx(U, 4, L + 8, C, 2048, "bf16")
+    states = []
+    for u in range(U):
+        labels = rng.integers(0, C, size=n)
+        labels[labels % 7 == 3] = 0          # some clusters stay empty, one gets big
+        sizes, offsets, perm = ck.build_csr(labels, C, 16)
+        mu = rng.standard_normal((C, d)).astype(np.float32).astype(np.float64)
+        states.append(dict(mu=mu, sizes=sizes, offsets=offsets, perm=perm))
+    upload_state(ctx, states, L)
+    scores = rng.integers(-20, 20, size=(U, C)).astype(np.float32)   # many ties
+    for B in (1, 700, 2048):
+        idx = torch.full((U, B), -1, dtype=torch.int32, device="cuda")
+        cnt = torch.empty(U, dtype=torch.int32, device="cuda")
+        ctx.select_scored(torch.from_numpy(scores).cuda(), B, idx, cnt)
+        for u in range(U):
+            st = states[u]
+            want, wc = ck.select(scores[u].astype(np.float64), st["sizes"], st["offsets"], st["perm"], B)
+            assert cnt[u].item() == wc
+            assert np.array_equal(idx[u, :wc].cpu().numpy(), want)
+    # fused path: its scores must rank like the GPU's own scores
+    q = torch.from_numpy(rng.standard_normal((U, 4, d))).to(torch.bfloat16).cuda()
+    sc = torch.empty(U, C, dtype=torch.float32, device="cuda")
+    ctx.score(q, sc)
+    i1 = torch.empty(U, 2048, dtype=torch.int32, device="cuda")
+    c1 = torch.empty(U, dtype=torch.int32, device="cuda")
+    i2, c2 = torch.empty_like(i1), torch.empty_like(c1)
+    ctx.select_scored(sc, 2048, i1, c1)
+    ctx.select(q, 2048, i2, c2)
+    # the fused kernel sums in the same order as ckv_score: identical selection
+    assert torch.equal(c1, c2)
+    for u in range(U):
+        assert torch.equal(i1[u, :c1[u]], i2[u, :c2[u]])
+    ctx.close()
