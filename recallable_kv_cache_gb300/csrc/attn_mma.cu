@@ -18,11 +18,10 @@
 //
 // Work split: the attended set of each unit is cut into tiles of 16 rows;
 // every warp owns a contiguous range of tiles (persistent grid, one CTA of 8
-// warps per SM).  Each warp runs its own 3-stage shared-memory ring: bulk
-// asynchronous copies (one per 256-byte row, completion counted on an
-// mbarrier) fill a stage while the warp computes an earlier one, token ids
-// are resolved four tiles ahead, rows sit at a 272-byte pitch so that ldmatrix
-// is free of bank conflicts.  The warp keeps an online softmax (max, sum,
+// warps per SM).  Each warp runs its own 3-stage shared-memory ring: 16-byte
+// cp.async copies (one commit group per tile) fill a stage while the warp
+// computes an earlier one, token ids are resolved four tiles ahead, and rows
+// sit at a 272-byte pitch so that ldmatrix is free of bank conflicts.  The warp keeps an online softmax (max, sum,
 // O^T) per unit and writes one partial per (unit, warp) when it leaves a
 // unit.  attn_mma_combine_kernel merges the partials of each unit in warp
 // order (deterministic, no atomics).
@@ -66,12 +65,20 @@ __device__ __forceinline__ void mma(float (&d)[4], uint32_t a0, uint32_t a1, uin
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
+// two floats -> packed bf16x2 (round to nearest even), lo in the low half
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-    const uint32_t l = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
-    const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
-    return l | (h << 16);
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
 }
-__device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+__device__ __forceinline__ float lo_of(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float hi_of(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+// 2^x with the hardware approximation (relative error below 2^-21); 2^-inf = 0
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 struct MmaArgs {
     const __nv_bfloat16* q;
@@ -99,7 +106,6 @@ template <int G>
 __global__ void __launch_bounds__(MW * 32, 1) attn_mma_kernel(const MmaArgs a) {
     constexpr int PW = G * (D + 2);
     extern __shared__ __align__(128) unsigned char mma_smem[];
-    __shared__ __align__(8) uint64_t full[MW][NST];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gw = blockIdx.x * MW + warp;
     const int t_begin = gw * a.tpw;
@@ -108,12 +114,6 @@ __global__ void __launch_bounds__(MW * 32, 1) attn_mma_kernel(const MmaArgs a) {
     unsigned char* wbase = mma_smem + (size_t)warp * NST * STAGE_BYTES;
     const uint32_t wbase_addr = ptx::smem_u32(wbase);
     const int pend = a.cur_len - a.clustered_end;
-    if (lane == 0) {
-#pragma unroll
-        for (int st = 0; st < NST; ++st) ptx::mbar_init(&full[warp][st], 1);
-        ptx::fence_barrier_init();
-    }
-    __syncwarp();
 
     // ---- token of row (lane & 15) of tile t, -1 if none (count cached per unit)
     int cu_ids = -1, r_ids = 0;
@@ -142,21 +142,27 @@ __global__ void __launch_bounds__(MW * 32, 1) attn_mma_kernel(const MmaArgs a) {
         return tok;
     };
     auto valid_bits = [&](int ids) -> unsigned { return __ballot_sync(FULL, ids >= 0) & 0xffffu; };
-    // bulk copies of the 16 K rows and 16 V rows of tile t into stage st;
-    // a missing row copies token 0 (a sink, always present) and is masked later
+    // 16-byte asynchronous copies of the 16 K rows and 16 V rows of tile t
+    // into stage st (lane l: chunk l % 16 of rows 2i + l / 16); a missing row
+    // copies token 0 (a sink, always present) so the stage holds finite values,
+    // and is masked later; one commit group per tile (empty past the range)
+    const int sub = lane >> 4, li = lane & 15;
     auto issue = [&](int st, int t, int ids) {
-        const int u = t / a.tpu;
-        uint64_t* bar = &full[warp][st];
-        if (lane == 0) ptx::mbar_arrive_expect_tx(bar, (uint32_t)STAGE_BYTES - 2u * TR * 16u);
-        __syncwarp();
-        if (lane < TR) {
-            const int tok = ids >= 0 ? ids : 0;
-            const size_t src = ((size_t)u * a.max_len + tok) * D;
-            unsigned char* dst = wbase + st * STAGE_BYTES + lane * PITCH;
-            ptx::fence_proxy_async_smem();
-            ptx::bulk_g2s(dst, a.K + src, D * 2, bar);
-            ptx::bulk_g2s(dst + TILE_BYTES, a.V + src, D * 2, bar);
+        if (t < t_end) {
+            const int u = t / a.tpu;
+            const __nv_bfloat16* Ku = a.K + (size_t)u * a.max_len * D + li * 8;
+            const __nv_bfloat16* Vu = a.V + (size_t)u * a.max_len * D + li * 8;
+            unsigned char* dst = wbase + st * STAGE_BYTES + li * 16;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int r = 2 * j + sub;
+                int tok = __shfl_sync(FULL, ids, r);
+                tok = tok >= 0 ? tok : 0;
+                ptx::cp_async16(dst + r * PITCH, Ku + (size_t)tok * D);
+                ptx::cp_async16(dst + TILE_BYTES + r * PITCH, Vu + (size_t)tok * D);
+            }
         }
+        ptx::cp_async_commit();
     };
 
     // ---- per-unit state (S^T layout: head = lane / 4; O^T accumulators:
@@ -217,18 +223,14 @@ __global__ void __launch_bounds__(MW * 32, 1) attn_mma_kernel(const MmaArgs a) {
     int ids_pend = ids_for(t_begin + 3);
     unsigned vb0 = valid_bits(ids0), vb1 = valid_bits(ids1), vb2 = valid_bits(ids2);
     issue(0, t_begin, ids0);
-    if (t_begin + 1 < t_end) issue(1, t_begin + 1, ids1);
-    if (t_begin + 2 < t_end) issue(2, t_begin + 2, ids2);
+    issue(1, t_begin + 1, ids1);  // tiles past t_end have no rows: empty groups
+    issue(2, t_begin + 2, ids2);
 
-    bool alive = true;
     for (int i = 0, t = t_begin; t < t_end; ++i, ++t) {
         const int st = i % NST;
         const int ids_next = ids_for(t + 4);  // in flight during this tile
-        if (!__all_sync(FULL, ptx::mbar_wait(&full[warp][st], (uint32_t)(i / NST) & 1u, WAIT_LIMIT, nullptr))) {
-            if (lane == 0 && a.dev_err) atomicCAS(a.dev_err, 0, CKV_DEV_TIMEOUT);
-            alive = false;
-            break;
-        }
+        ptx::cp_async_wait_group<NST - 1>();  // this lane's copies of tile t have landed
+        __syncwarp();                          // ... and every other lane's
         const unsigned valid = vb0;
         const int u = t / a.tpu;
         if (u != cur_u) {
@@ -266,25 +268,33 @@ __global__ void __launch_bounds__(MW * 32, 1) attn_mma_kernel(const MmaArgs a) {
             tm = fmaxf(tm, __shfl_xor_sync(FULL, tm, 1));
             tm = fmaxf(tm, __shfl_xor_sync(FULL, tm, 2));
             const float mnew = fmaxf(mrun, tm);
-            const float sc = (mnew == -INFINITY) ? 1.f : exp2f(mrun - mnew);
+            // -inf - -inf is avoided: ex2(-inf) = 0 covers masked rows
+            const float msub = (mnew == -INFINITY) ? 0.f : mnew;
             float p[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) p[e] = (v[e] == -INFINITY) ? 0.f : exp2f(v[e] - mnew);
+            for (int e = 0; e < 4; ++e) p[e] = ex2(v[e] - msub);
+            const bool grew = mnew != mrun;
+            const float sc = grew ? ex2(mrun - msub) : 1.f;
             lrun = lrun * sc + ((p[0] + p[1]) + (p[2] + p[3]));
             mrun = mnew;
-            const float h00 = bf16_round(p[0]), h01 = bf16_round(p[1]);
-            const float h10 = bf16_round(p[2]), h11 = bf16_round(p[3]);
-            const uint32_t bh0 = pack2(h00, h01), bh1 = pack2(h10, h11);
-            const uint32_t bl0 = pack2(p[0] - h00, p[1] - h01), bl1 = pack2(p[2] - h10, p[3] - h11);
-            const float sc0 = __shfl_sync(FULL, sc, ((lane & 3) * 2) * 4);
-            const float sc1 = __shfl_sync(FULL, sc, ((lane & 3) * 2 + 1) * 4);
+            const uint32_t bh0 = pack2(p[0], p[1]), bh1 = pack2(p[2], p[3]);
+            const uint32_t bl0 = pack2(p[0] - lo_of(bh0), p[1] - hi_of(bh0));
+            const uint32_t bl1 = pack2(p[2] - lo_of(bh1), p[3] - hi_of(bh1));
+            // rescale the O^T columns only when some head's running max moved
+            if (__any_sync(FULL, grew)) {
+                const float sc0 = __shfl_sync(FULL, sc, ((lane & 3) * 2) * 4);
+                const float sc1 = __shfl_sync(FULL, sc, ((lane & 3) * 2 + 1) * 4);
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) {
+                    o[mt][0] *= sc0;
+                    o[mt][1] *= sc1;
+                    o[mt][2] *= sc0;
+                    o[mt][3] *= sc1;
+                }
+            }
             const int vrow = ((lane >> 3) >> 1) * 8 + (lane & 7);
 #pragma unroll
             for (int mt = 0; mt < 8; ++mt) {
-                o[mt][0] *= sc0;
-                o[mt][1] *= sc1;
-                o[mt][2] *= sc0;
-                o[mt][3] *= sc1;
                 const int chunk = 2 * mt + ((lane >> 3) & 1);
                 uint32_t a0, a1, a2, a3;
                 ldsm_x4_t(vbs + (uint32_t)(vrow * PITCH + chunk * 16), a0, a1, a2, a3);
@@ -293,14 +303,15 @@ __global__ void __launch_bounds__(MW * 32, 1) attn_mma_kernel(const MmaArgs a) {
             }
         }
         __syncwarp();
-        // the stage is free again: tile t + NST into it
-        if (t + NST < t_end) issue(st, t + NST, ids_pend);
+        // the stage is free again: tile t + NST into it (an empty group past the end)
+        issue(st, t + NST, ids_pend);
         vb0 = vb1;
         vb1 = vb2;
         vb2 = valid_bits(ids_pend);
         ids_pend = ids_next;
     }
-    if (alive && cur_u >= 0) flush(cur_u);
+    ptx::cp_async_wait_all();
+    if (cur_u >= 0) flush(cur_u);
 }
 
 // One CTA per unit, one thread per output (head, channel): merge the unit's

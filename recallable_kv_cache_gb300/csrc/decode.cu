@@ -202,57 +202,180 @@ __global__ void __launch_bounds__(1024, 1) sel_kernel(
     }
     __syncthreads();
 
-    // ---- 3. bitonic sort, ascending keys; position i = e * NT + tid
-    uint64_t kv[E];
+    // ---- 3. exact candidate pre-filter: a size-weighted histogram over the
+    // top 12 bits of the keys (ascending key = descending score) gives the
+    // first bin at which the cumulative size reaches min(B, total).  Clusters
+    // in earlier bins rank before every cluster of that bin, clusters in later
+    // bins after all of them, and the candidates (bins up to and including
+    // that one) already hold at least the budget: only they need ranking.
+    constexpr int HBITS = 12, NBIN = 1 << HBITS;
+    int32_t* hist = offc + N;                                 // [NBIN]
+    uint64_t* cand = reinterpret_cast<uint64_t*>(start);      // [<= NT] (start/cl reused)
+    __shared__ int32_t s_bstar, s_total, s_M;
+    for (int i = tid; i < NBIN; i += NT) hist[i] = 0;
+    if (tid == 0) s_M = 0;
+    __syncthreads();
+    for (int c = tid; c < C; c += NT) atomicAdd(&hist[(int)(sk[c] >> (64 - HBITS))], szc[c]);
+    __syncthreads();
+    {
+        // block-wide: thread t owns bins [t*PER, t*PER + PER) (NT * PER == NBIN)
+        const int PER = NBIN / NT;
+        int ls = 0;
+        for (int i = 0; i < PER; ++i) ls += hist[tid * PER + i];
+        int incl = ls;
 #pragma unroll
-    for (int e = 0; e < E; ++e) kv[e] = sk[e * NT + tid];
-    for (int k = 2; k <= N; k <<= 1) {
-        for (int j = k >> 1; j > 0; j >>= 1) {
-            if (j >= NT) {
-                const int ej = j / NT;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(FULL, incl, o);
+            if (lane >= o) incl += t;
+        }
+        if (lane == 31) wsum[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            const int wt = lane < nwarps ? wsum[lane] : 0;
+            int wi = wt;
 #pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    if (e & ej) continue;
-                    const int pe = e | ej;
-                    const int i = e * NT + tid;
-                    const bool up = (i & k) == 0;
-                    const uint64_t x = kv[e], y = kv[pe];
-                    if ((x > y) == up) {
-                        kv[e] = y;
-                        kv[pe] = x;
-                    }
-                }
-            } else if (j >= 32) {
-                __syncthreads();
-#pragma unroll
-                for (int e = 0; e < E; ++e) sk[e * NT + tid] = kv[e];
-                __syncthreads();
-#pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    const int i = e * NT + tid;
-                    const uint64_t p = sk[i ^ j];
-                    const bool keep_min = ((i & j) == 0) == ((i & k) == 0);
-                    kv[e] = keep_min ? (kv[e] < p ? kv[e] : p) : (kv[e] < p ? p : kv[e]);
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    const int i = e * NT + tid;
-                    const uint64_t p = __shfl_xor_sync(FULL, kv[e], j);
-                    const bool keep_min = ((i & j) == 0) == ((i & k) == 0);
-                    kv[e] = keep_min ? (kv[e] < p ? kv[e] : p) : (kv[e] < p ? p : kv[e]);
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(FULL, wi, o);
+                if (lane >= o) wi += t;
+            }
+            if (lane < nwarps) wsum[lane] = wi - wt;
+            if (lane == 31) s_total = wi;
+            if (lane == 0) s_bstar = -1;
+        }
+        __syncthreads();
+        const int tot = s_total;
+        const int target = tot < B ? tot : B;
+        const int excl = wsum[warp] + incl - ls;  // bins before this thread's
+        if (target > 0 && excl < target && excl + ls >= target) {
+            int run = excl;
+            for (int i = 0; i < PER; ++i) {
+                run += hist[tid * PER + i];
+                if (run >= target) {
+                    s_bstar = tid * PER + i;  // exactly one thread crosses the target
+                    break;
                 }
             }
         }
     }
+    __syncthreads();
+    const int total = s_total, bstar = s_bstar;
+    // every cluster needs ranking when the budget covers all tokens
+    const bool take_all = total <= B;
+    if (!take_all) {
+        for (int c0 = 0; c0 < C; c0 += NT) {  // c0 is warp-uniform: the ballot sees all lanes
+            const int c = c0 + tid;
+            const bool is_c = c < C && (int)(sk[c] >> (64 - HBITS)) <= bstar;
+            const unsigned bal = __ballot_sync(FULL, is_c);
+            int wbase = 0;
+            if (lane == 0 && bal) wbase = atomicAdd(&s_M, __popc(bal));
+            wbase = __shfl_sync(FULL, wbase, 0);
+            if (is_c) {
+                const int pos = wbase + __popc(bal & ((1u << lane) - 1u));
+                if (pos < NT) cand[pos] = sk[c];
+            }
+        }
+    }
+    __syncthreads();
+    const int M = s_M;
+    const bool small = !take_all && M <= NT;
+    int nsorted;
+    if (small && M <= 32) {
+        // ---- 3a. up to 32 candidates: one warp, shuffles only
+        if (warp == 0) {
+            uint64_t ck = (lane < M) ? cand[lane] : ~0ull;
+            for (int k = 2; k <= 32; k <<= 1)
+                for (int j = k >> 1; j > 0; j >>= 1) {
+                    const uint64_t p = __shfl_xor_sync(FULL, ck, j);
+                    const bool keep_min = ((lane & j) == 0) == ((lane & k) == 0);
+                    ck = keep_min ? (ck < p ? ck : p) : (ck < p ? p : ck);
+                }
+            if (lane < M) sk[lane] = ck;
+        }
+        nsorted = M;
+    } else if (small) {
+        // ---- 3b. sort the M candidates: one key per thread below N2
+        int N2 = 32;
+        while (N2 < M) N2 <<= 1;
+        uint64_t ck = (tid < M) ? cand[tid] : ~0ull;
+        for (int k = 2; k <= N2; k <<= 1) {
+            for (int j = k >> 1; j > 0; j >>= 1) {
+                if (j >= 32) {
+                    __syncthreads();
+                    if (tid < N2) cand[tid] = ck;
+                    __syncthreads();
+                    if (tid < N2) {
+                        const uint64_t p = cand[tid ^ j];
+                        const bool keep_min = ((tid & j) == 0) == ((tid & k) == 0);
+                        ck = keep_min ? (ck < p ? ck : p) : (ck < p ? p : ck);
+                    }
+                } else {
+                    const uint64_t p = __shfl_xor_sync(FULL, ck, j);
+                    const bool keep_min = ((tid & j) == 0) == ((tid & k) == 0);
+                    ck = keep_min ? (ck < p ? ck : p) : (ck < p ? p : ck);
+                }
+            }
+        }
+        __syncthreads();
+        if (tid < M) sk[tid] = ck;
+        nsorted = M;
+    } else {
+        // ---- 3c. full bitonic sort, ascending keys; position i = e * NT + tid
+        uint64_t kv[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) kv[e] = sk[e * NT + tid];
+        for (int k = 2; k <= N; k <<= 1) {
+            for (int j = k >> 1; j > 0; j >>= 1) {
+                if (j >= NT) {
+                    const int ej = j / NT;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        if (e & ej) continue;
+                        const int pe = e | ej;
+                        const int i = e * NT + tid;
+                        const bool up = (i & k) == 0;
+                        const uint64_t x = kv[e], y = kv[pe];
+                        if ((x > y) == up) {
+                            kv[e] = y;
+                            kv[pe] = x;
+                        }
+                    }
+                } else if (j >= 32) {
+                    __syncthreads();
+#pragma unroll
+                    for (int e = 0; e < E; ++e) sk[e * NT + tid] = kv[e];
+                    __syncthreads();
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        const int i = e * NT + tid;
+                        const uint64_t p = sk[i ^ j];
+                        const bool keep_min = ((i & j) == 0) == ((i & k) == 0);
+                        kv[e] = keep_min ? (kv[e] < p ? kv[e] : p) : (kv[e] < p ? p : kv[e]);
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        const int i = e * NT + tid;
+                        const uint64_t p = __shfl_xor_sync(FULL, kv[e], j);
+                        const bool keep_min = ((i & j) == 0) == ((i & k) == 0);
+                        kv[e] = keep_min ? (kv[e] < p ? kv[e] : p) : (kv[e] < p ? p : kv[e]);
+                    }
+                }
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < E; ++e) sk[e * NT + tid] = kv[e];
+        nsorted = C;
+    }
+    __syncthreads();
 
-    // ---- 4. sizes in rank order, exclusive prefix sum over positions
+    // ---- 4. sizes in rank order, exclusive prefix sum over the ranked keys
     int base = 0;
 #pragma unroll
     for (int e = 0; e < E; ++e) {
         const int i = e * NT + tid;
-        const int c = (int)(uint32_t)kv[e];
-        const int sz = i < C ? szc[c] : 0;
+        const int c = i < nsorted ? (int)(uint32_t)sk[i] : 0;
+        const int sz = i < nsorted ? szc[c] : 0;
         int incl = sz;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -277,20 +400,19 @@ __global__ void __launch_bounds__(1024, 1) sel_kernel(
         const int excl = base + wsum[warp] + incl - sz;
         __syncthreads();
         start[i] = excl;
-        cl[i] = i < C ? c : 0;
+        cl[i] = c;
         base += seg_total;
         __syncthreads();
     }
 
     // ---- 5. cut at the budget and compact the token ids
-    const int total = base;
     const int cnt = total < B ? total : B;
     if (tid == 0) count[u] = cnt;
     const int32_t* pu = perm + (size_t)u * ntok;
     int32_t* out = idx + (size_t)u * B;
     for (int p = tid; p < cnt; p += NT) {
-        // largest rank r < C with start[r] <= p (that cluster is non-empty and holds p)
-        int lo = 0, hi = C - 1;
+        // largest rank r with start[r] <= p (that cluster is non-empty and holds p)
+        int lo = 0, hi = nsorted - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
             if (start[mid] <= p) lo = mid;
@@ -819,7 +941,7 @@ cudaError_t launch_score(const ckv_ctx* ctx, const void* q, int C, float* scores
 template <typename T, int G, int E, bool FS>
 cudaError_t launch_sel_t(const ckv_ctx* ctx, const void* q, const float* scores, int stride, int C, int N,
                          int B, int32_t* idx, int32_t* count, cudaStream_t s) {
-    const size_t smem = (size_t)N * 24;
+    const size_t smem = (size_t)N * 24 + (size_t)4096 * 4;
     auto kern = sel_kernel<T, G, E, FS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
