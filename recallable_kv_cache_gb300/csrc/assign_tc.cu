@@ -15,9 +15,10 @@
 //   warp 1     TMEM owner and MMA issuer: per tile and per column chunk of at
 //              most 256 centroids, 8 x tcgen05.mma (K = 16 each) into one of
 //              two 256-column TMEM slots;
-//   warps 2-5  epilogue: tcgen05.ld of the fp32 dots (one TMEM lane = one
-//              token), running arg-max in increasing centroid order with a
-//              strict '>' (ties keep the lower index), label store.
+//   warps 2-9  epilogue: tcgen05.ld of the fp32 dots (one TMEM lane = one
+//              token; two warps per lane quarter split the 32-column groups),
+//              running arg-max in increasing centroid order with a strict '>'
+//              (ties keep the lower index), pair merge, label store.
 // All mbarrier waits are bounded; a timeout sets the device error word and
 // every role leaves its loop.
 #include <cuda.h>
@@ -35,7 +36,7 @@ namespace {
 constexpr int A_STAGE_BYTES = ASSIGN_TILE * D * 2;  // 32 KB: two 64-column panels
 constexpr int A_PANEL_BYTES = ASSIGN_TILE * 128;    // 16 KB
 constexpr int B_BOX_ROWS = 32;
-constexpr int THREADS = 192;
+constexpr int THREADS = 320;  // producer, MMA issuer, 8 epilogue warps
 
 struct AssignArgs {
     int n;              // clustered tokens per unit
@@ -58,6 +59,10 @@ struct __align__(8) Bars {
     uint64_t b_empty;
     uint64_t tm_full[2];
     uint64_t tm_empty[2];
+    uint64_t pair_full[4];   // per TMEM lane quarter: second-half partials written
+    uint64_t pair_free[4];   // ... and consumed
+    float xbest[4][32];
+    int xarg[4][32];
     uint32_t tmem_base;
     int abort;
 };
@@ -93,7 +98,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         ptx::mbar_init(&bs->b_empty, 1);
         for (int s = 0; s < 2; ++s) {
             ptx::mbar_init(&bs->tm_full[s], 1);
-            ptx::mbar_init(&bs->tm_empty[s], 4);
+            ptx::mbar_init(&bs->tm_empty[s], 8);
+        }
+        for (int qq = 0; qq < 4; ++qq) {
+            ptx::mbar_init(&bs->pair_full[qq], 1);
+            ptx::mbar_init(&bs->pair_free[qq], 1);
         }
         bs->abort = 0;
         ptx::fence_barrier_init();
@@ -182,13 +191,21 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
-        int item = 0;
+        // warps 2..9: two per TMEM lane quarter (warp % 4); the first of a pair
+        // takes the even 32-column groups of every chunk, the second the odd
+        // ones.  Each warp issues all its TMEM loads of a chunk (at most four
+        // groups) before one wait.  Per row the pair's partial arg-maxes are
+        // merged through shared memory; ties keep the lower column.
+        const int q = warp & 3;
+        const int half = (warp - 2) >> 2;
+        int item = 0, ntile = 0;
         bool alive = true;
-        for (int t = t_begin; t < t_end && alive; ++t) {
+        for (int t = t_begin; t < t_end && alive; ++t, ++ntile) {
             const int u = t / p.tiles_per_unit, tl = t % p.tiles_per_unit;
-            float best = -INFINITY;
-            int arg = 0;
+            // four independent running maxima (columns j mod 4) break the
+            // compare-select dependency chain; merged below
+            float bk[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            int ak[4] = {0, 0, 0, 0};
             for (int ch = 0; ch < p.nchunk; ++ch, ++item) {
                 const int slot = item & 1;
                 const bool ok = __all_sync(
@@ -200,28 +217,37 @@ __global__ void __launch_bounds__(THREADS, 1)
                 ptx::tc_fence_after();
                 const int c0 = 256 * ch;
                 const int nvalid = min(256, p.C - c0);
+                const int ngroups = (nvalid + 31) >> 5;
                 const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)slot * 256u;
-                for (int g0 = 0; g0 < nvalid; g0 += 32) {
-                    uint32_t r[32];
-                    ptx::tmem_ld32(taddr + (uint32_t)g0, r);
-                    ptx::tmem_ld_wait();
-                    const int lim = nvalid - g0;
+                uint32_t r[4][32];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int g = 2 * k + half;
+                    if (g < ngroups) ptx::tmem_ld32(taddr + (uint32_t)(g * 32), r[k]);
+                }
+                ptx::tmem_ld_wait();
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int g = 2 * k + half;
+                    if (g >= ngroups) break;
+                    const int lim = nvalid - g * 32;
+                    const int cb = c0 + g * 32;
                     if (lim >= 32) {
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
-                            const float v = __uint_as_float(r[j]);
-                            if (v > best) {
-                                best = v;
-                                arg = c0 + g0 + j;
+                            const float v = __uint_as_float(r[k][j]);
+                            if (v > bk[j & 3]) {
+                                bk[j & 3] = v;
+                                ak[j & 3] = cb + j;
                             }
                         }
                     } else {
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
-                            const float v = __uint_as_float(r[j]);
-                            if (j < lim && v > best) {
-                                best = v;
-                                arg = c0 + g0 + j;
+                            const float v = __uint_as_float(r[k][j]);
+                            if (j < lim && v > bk[j & 3]) {
+                                bk[j & 3] = v;
+                                ak[j & 3] = cb + j;
                             }
                         }
                     }
@@ -231,8 +257,41 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (lane == 0) ptx::mbar_arrive(&bs->tm_empty[slot]);
             }
             if (!alive) break;
-            const int row = tl * ASSIGN_TILE + q * 32 + lane;
-            if (row < p.n) p.labels[(size_t)u * p.n + row] = arg;
+            // each chain holds its first maximum; (larger value, then lower
+            // column) over chains and over the pair picks the row's first maximum
+            float best = bk[0];
+            int arg = ak[0];
+#pragma unroll
+            for (int k = 1; k < 4; ++k)
+                if (bk[k] > best || (bk[k] == best && ak[k] < arg)) {
+                    best = bk[k];
+                    arg = ak[k];
+                }
+            if (half == 1) {
+                if (ntile > 0 && !__all_sync(0xffffffffu, wait_or_abort(&bs->pair_free[q], (ntile - 1) & 1, bs, p.dev_err))) {
+                    alive = false;
+                    break;
+                }
+                bs->xbest[q][lane] = best;
+                bs->xarg[q][lane] = arg;
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&bs->pair_full[q]);
+            } else {
+                if (!__all_sync(0xffffffffu, wait_or_abort(&bs->pair_full[q], ntile & 1, bs, p.dev_err))) {
+                    alive = false;
+                    break;
+                }
+                const float ob = bs->xbest[q][lane];
+                const int oa = bs->xarg[q][lane];
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&bs->pair_free[q]);
+                if (ob > best || (ob == best && oa < arg)) {
+                    best = ob;
+                    arg = oa;
+                }
+                const int row = tl * ASSIGN_TILE + q * 32 + lane;
+                if (row < p.n) p.labels[(size_t)u * p.n + row] = arg;
+            }
         }
     }
 

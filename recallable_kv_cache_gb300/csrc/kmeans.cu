@@ -240,12 +240,18 @@ __global__ void __launch_bounds__(1024) csr_scan_kernel(int n, int C, int cmax, 
     __shared__ int32_t wb[33];
     const int u = blockIdx.x, tid = threadIdx.x;
     for (int c = tid; c < C; c += 1024) {
+        // chunk counts of cluster c -> exclusive prefix over chunks, 16 loads in flight
         int run = 0;
-        for (int k = 0; k < nchunk; ++k) {
-            int32_t* p = chunk_cnt + ((size_t)u * nchunk + k) * cmax + c;
-            const int v = *p;
-            *p = run;
-            run += v;
+        int32_t* col = chunk_cnt + (size_t)u * nchunk * cmax + c;
+        for (int k0 = 0; k0 < nchunk; k0 += 16) {
+            int v[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = (k0 + j < nchunk) ? col[(size_t)(k0 + j) * cmax] : 0;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                if (k0 + j < nchunk) col[(size_t)(k0 + j) * cmax] = run;
+                run += v[j];
+            }
         }
         sizes[(size_t)u * cmax + c] = run;
         off[c] = run;
