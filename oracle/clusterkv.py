@@ -20,7 +20,7 @@ algorithm out step by step, in float64, in the order the page gives it:
   * the exact objective (top-B by q.k)       - section "Problem formulation and
     design principle".
 
-Readings of points the page leaves open (each also listed in the design doc):
+Readings of points the page leaves open:
   * C = floor((L - 16) / 80): the 16 sink tokens are not counted in L/80.
   * Seeding ("randomly sample keys as initial centroids") is read as the
     deterministic stride pick mu_j = k[s*j], s = min(80, floor(n / C)).
