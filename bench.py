@@ -34,6 +34,15 @@ import torch  # noqa: E402
 from recallable_kv_cache_gb300 import synth  # noqa: E402
 
 METRIC = "sparse-decode tokens/s at 32k ctx, B=1024; K-means ms/layer; % of HBM roofline"
+
+# DRAM bytes (read + write) of one attn_mma_kernel launch per algorithmic byte,
+# from one ncu capture of the current kernel on this workload (decode step 41:
+# 146.7 MB of DRAM traffic for 143.5 MB of algorithmic bytes).  The traffic of a
+# launch is this ratio times its algorithmic bytes (both grow with the attended
+# rows).  Set to None whenever the kernel changes until it is captured again.
+ATTN_TRAFFIC_PER_ALG_BYTE = 146.745 / 143.53
+ATTN_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch (decode step 41, "
+                       "146.7 MB for 143.5 MB algorithmic), scaled to the mean launch by algorithmic bytes")
 WORKLOAD = "decode_32k"
 
 
@@ -247,12 +256,31 @@ def run_ours(args, w, rank, world, device):
                launches=(launches["prefill"] + launches["decode"]) * args.steps)
     res["attn_bytes_per_launch"] = statistics.mean(decode_bytes(w, t, C_at[t])[0] for t in sampled)
     res["decode_bytes_per_step"] = sum(decode_bytes(w, t, C_at[t])[1] for t in range(T)) / T
+    res["assign_ms"] = time_assign(ctx, w, K)
     res["w"] = w
     res["ctx"] = ctx
     res["tensors"] = (K, V, Q)
     if not args.no_e2e:
         res["e2e"] = run_e2e(ctx, w, K, V, Q)
     return res
+
+
+def time_assign(ctx, w, K, reps=5):
+    """The tensor-core assignment kernel timed alone (outside the timed job):
+    one K-means assignment pass over every unit's prompt keys against the
+    prefill centroids, CUDA events on the launching stream."""
+    ctx.cluster_prefill(K, w.L, w.C)  # back to the prefill clusters (C of the prompt)
+    lab = torch.empty(w.units, w.L - w.sinks, dtype=torch.int32, device="cuda")
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(3):
+        ctx.kmeans_assign(K, w.L, lab)
+    torch.cuda.synchronize()
+    a0.record()
+    for _ in range(reps):
+        ctx.kmeans_assign(K, w.L, lab)
+    a1.record()
+    torch.cuda.synchronize()
+    return a0.elapsed_time(a1) / reps
 
 
 def run_e2e(ctx, w, K, V, Q):
@@ -415,6 +443,7 @@ def main():
     attn_gbs = r["attn_bytes_per_launch"] / (r["attn_ms"] / 1000.0) / 1e9
     decode_gbs = r["decode_bytes_per_step"] / (decode_ms / T / 1000.0) / 1e9
     kflops, kbytes = kmeans_flops_bytes(w)
+    assign_flops = kflops / w.iters
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
@@ -428,12 +457,21 @@ def main():
         "kmeans_roofline": {"tflops": kflops / (prefill_ms / 1000.0) / 1e12,
                             "peak_tflops": meas.get("bf16_tflops_sustained", 1700.0),
                             "bytes_gbs": kbytes / (prefill_ms / 1000.0) / 1e9},
-        "roofline": {"bound": "hbm", "kernel": "attn_kernel (gather + split-K attention)",
+        "roofline": {"bound": "hbm", "kernel": "attn_mma_kernel + attn_mma_combine_kernel (gather + "
+                                               "split-K attention)",
                      "achieved": attn_gbs, "peak": hbm, "unit": "GB/s", "frac": attn_gbs / hbm,
-                     "traffic": None, "bytes_per_launch": r["attn_bytes_per_launch"],
+                     "traffic": (ATTN_TRAFFIC_PER_ALG_BYTE * r["attn_bytes_per_launch"]
+                                 if ATTN_TRAFFIC_PER_ALG_BYTE else None),
+                     "traffic_source": ATTN_TRAFFIC_SOURCE,
+                     "bytes_per_launch": r["attn_bytes_per_launch"],
                      "launch_us": 1000.0 * r["attn_ms"], "peak_kind": peak_kind,
                      "timing": "CUDA events around the attention launch (+ its combine kernel) of "
                                "every 16th decode step, inside the timed graph"},
+        "assign_roofline": {"bound": "tensor", "kernel": "assign_tc_kernel",
+                            "achieved": assign_flops / (r["assign_ms"] / 1000.0) / 1e12,
+                            "peak": meas.get("bf16_tflops", 1900.0), "unit": "TFLOP/s",
+                            "frac": assign_flops / (r["assign_ms"] / 1000.0) / 1e12 / meas.get("bf16_tflops", 1900.0),
+                            "launch_us": 1000.0 * r["assign_ms"], "peak_kind": peak_kind + " (burst: timed alone)"},
         "phase_ms": {"prefill_clustering": prefill_ms, "decode_loop": decode_ms},
         "per_launch_us": {"select": 1000.0 * r["select_ms"], "attention": 1000.0 * r["attn_ms"]},
         "gpu_launches": r["launches"], "clocks": r["clocks"],

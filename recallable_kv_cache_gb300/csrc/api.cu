@@ -11,7 +11,6 @@
 
 namespace ckv {
 size_t assign_tc_smem(int cpad, int* stages_out);
-size_t incremental_smem(int m);
 }  // namespace ckv
 
 using namespace ckv;
@@ -35,7 +34,7 @@ cudaError_t alloc(T** p, size_t count) {
 void free_all(ckv_ctx* c) {
     void* ptrs[] = {c->mu32,   c->mu_s == c->mu32 ? nullptr : c->mu_s, c->mu_hat, c->sizes,
                     c->offsets, c->perm, c->labels, c->chunk_cnt, c->task_off, c->task_cl,
-                    c->seg_part, c->scores, c->attn_part, c->attn_cnt, c->dev_err};
+                    c->seg_part, c->scores, c->attn_part, c->attn_cnt, c->dev_err, c->assign_best};
     for (void* p : ptrs)
         if (p) cudaFree(p);
 }
@@ -127,6 +126,8 @@ ckv_status ckv_create(const ckv_config* cfg, ckv_ctx** out) {
     ok = ok && alloc(&c->attn_part, U * c->max_splits * cfg->g * (D + 2)) == cudaSuccess;
     ok = ok && alloc(&c->attn_cnt, U) == cudaSuccess;
     ok = ok && alloc(&c->dev_err, 1) == cudaSuccess;
+    if (cfg->kv_dtype == CKV_BF16 && c->cmax_pad > MAX_ASSIGN_CPAD)
+        ok = ok && alloc(&c->assign_best, U * c->ntok) == cudaSuccess;
     if (ok) {
         const size_t hat = U * (size_t)c->cmax_pad * D * c->elem;
         ok = cudaMemset(c->mu_hat, 0, hat) == cudaSuccess && cudaMemset(c->attn_cnt, 0, U * 4) == cudaSuccess &&

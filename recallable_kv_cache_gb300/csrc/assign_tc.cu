@@ -9,9 +9,15 @@
 // normalisation is folded away and the raw bf16 keys feed the MMA directly.
 //
 // One persistent CTA per SM walks a contiguous range of 128-token tiles
-// (flattened over units).  Warp roles:
-//   warp 0     TMA producer: the unit's mu_hat [cpad x 128] once per unit
-//              (resident in smem), key tiles [128 x 128] through a ring;
+// (flattened over units).  The unit's centroid directions stay resident in
+// shared memory while its tiles stream by; when there are too many of them
+// (more than 640 rows), they are split into passes of at most 512 rows: the
+// CTA walks its tiles of the unit once per pass, and the running maximum of a
+// token and its column are kept in global memory between passes (a later pass
+// wins only with a strictly larger dot, so ties still go to the lower index).
+// Warp roles:
+//   warp 0     TMA producer: the pass's rows of mu_hat [<= 640 x 128] once per
+//              (unit, pass), key tiles [128 x 128] through a ring;
 //   warp 1     TMEM owner and MMA issuer: per tile and per column chunk of at
 //              most 256 centroids, 8 x tcgen05.mma (K = 16 each) into one of
 //              two 256-column TMEM slots;
@@ -42,13 +48,15 @@ struct AssignArgs {
     int n;              // clustered tokens per unit
     int C;              // centroids
     int cpad;           // C rounded up to 32
-    int nchunk;         // column chunks per tile (ceil(cpad / 256))
+    int pw;             // centroid rows per pass (multiple of 32)
+    int npass;          // passes over a unit's tiles: ceil(cpad / pw)
     int tiles_per_unit;
     int total_tiles;
     int tiles_per_cta;
     int sinks;
     int stages;
     int32_t* labels;
+    float* best;        // [units][n] running maxima between passes (npass > 1)
     int32_t* dev_err;
 };
 
@@ -82,8 +90,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     unsigned char* A = smem;                                     // stages x 32 KB
-    unsigned char* Bm = smem + (size_t)p.stages * A_STAGE_BYTES;  // 2 panels x cpad x 128 B
-    Bars* bs = reinterpret_cast<Bars*>(Bm + (size_t)p.cpad * 256);
+    unsigned char* Bm = smem + (size_t)p.stages * A_STAGE_BYTES;  // 2 panels x pw x 128 B
+    Bars* bs = reinterpret_cast<Bars*>(Bm + (size_t)p.pw * 256);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t_begin = blockIdx.x * p.tiles_per_cta;
@@ -121,29 +129,39 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) {
             ptx::prefetch_tmap(&tmK);
             ptx::prefetch_tmap(&tmMu);
-            int cur_unit = -1, b_loads = 0;
-            for (int t = t_begin, it = 0; t < t_end; ++t, ++it) {
-                const int u = t / p.tiles_per_unit, tl = t % p.tiles_per_unit;
-                if (u != cur_unit) {
-                    if (cur_unit >= 0 && !wait_or_abort(&bs->b_empty, (b_loads - 1) & 1, bs, p.dev_err))
+            int b_loads = 0, it = 0;
+            bool alive = true;
+            for (int t0 = t_begin; t0 < t_end && alive;) {
+                const int u = t0 / p.tiles_per_unit;
+                const int t1 = min(t_end, (u + 1) * p.tiles_per_unit);
+                for (int ps = 0; ps < p.npass && alive; ++ps) {
+                    const int prow = ps * p.pw;
+                    const int rows = min(p.pw, p.cpad - prow);
+                    if (b_loads > 0 && !wait_or_abort(&bs->b_empty, (b_loads - 1) & 1, bs, p.dev_err)) {
+                        alive = false;
                         break;
-                    ptx::mbar_arrive_expect_tx(&bs->b_full, (uint32_t)p.cpad * 256u);
+                    }
+                    ptx::mbar_arrive_expect_tx(&bs->b_full, (uint32_t)rows * 256u);
                     for (int pn = 0; pn < 2; ++pn)
-                        for (int r0 = 0; r0 < p.cpad; r0 += B_BOX_ROWS)
-                            ptx::tma_load_3d(Bm + (size_t)pn * p.cpad * 128 + (size_t)r0 * 128, &tmMu,
-                                             pn * 64, r0, u, &bs->b_full);
+                        for (int r0 = 0; r0 < rows; r0 += B_BOX_ROWS)
+                            ptx::tma_load_3d(Bm + (size_t)pn * p.pw * 128 + (size_t)r0 * 128, &tmMu, pn * 64,
+                                             prow + r0, u, &bs->b_full);
                     ++b_loads;
-                    cur_unit = u;
+                    for (int t = t0; t < t1; ++t, ++it) {
+                        const int s = it % p.stages;
+                        if (it >= p.stages &&
+                            !wait_or_abort(&bs->a_empty[s], ((it / p.stages) - 1) & 1, bs, p.dev_err)) {
+                            alive = false;
+                            break;
+                        }
+                        unsigned char* a = A + (size_t)s * A_STAGE_BYTES;
+                        ptx::mbar_arrive_expect_tx(&bs->a_full[s], A_STAGE_BYTES);
+                        const int row = p.sinks + (t - u * p.tiles_per_unit) * ASSIGN_TILE;
+                        ptx::tma_load_3d(a, &tmK, 0, row, u, &bs->a_full[s]);
+                        ptx::tma_load_3d(a + A_PANEL_BYTES, &tmK, 64, row, u, &bs->a_full[s]);
+                    }
                 }
-                const int s = it % p.stages;
-                if (it >= p.stages &&
-                    !wait_or_abort(&bs->a_empty[s], ((it / p.stages) - 1) & 1, bs, p.dev_err))
-                    break;
-                unsigned char* a = A + (size_t)s * A_STAGE_BYTES;
-                ptx::mbar_arrive_expect_tx(&bs->a_full[s], A_STAGE_BYTES);
-                const int row = p.sinks + tl * ASSIGN_TILE;
-                ptx::tma_load_3d(a, &tmK, 0, row, u, &bs->a_full[s]);
-                ptx::tma_load_3d(a + A_PANEL_BYTES, &tmK, 64, row, u, &bs->a_full[s]);
+                t0 = t1;
             }
         }
     } else if (warp == 1) {
@@ -151,42 +169,57 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) {
             const uint32_t a_base = ptx::smem_u32(A);
             const uint32_t b_base = ptx::smem_u32(Bm);
-            int cur_unit = -1, b_loads = 0, item = 0;
+            int b_loads = 0, it = 0, item = 0;
             bool alive = true;
-            for (int t = t_begin, it = 0; t < t_end && alive; ++t, ++it) {
-                const int u = t / p.tiles_per_unit;
-                if (u != cur_unit) {
-                    if (cur_unit >= 0) ptx::mma_commit(&bs->b_empty);
-                    if (!wait_or_abort(&bs->b_full, b_loads & 1, bs, p.dev_err)) break;
-                    ++b_loads;
-                    cur_unit = u;
-                }
-                const int s = it % p.stages;
-                if (!wait_or_abort(&bs->a_full[s], (it / p.stages) & 1, bs, p.dev_err)) break;
-                ptx::tc_fence_after();
-                const uint32_t a_st = a_base + (uint32_t)s * A_STAGE_BYTES;
-                for (int ch = 0; ch < p.nchunk; ++ch, ++item) {
-                    const int slot = item & 1;
-                    if (item >= 2 &&
-                        !wait_or_abort(&bs->tm_empty[slot], ((item >> 1) - 1) & 1, bs, p.dev_err)) {
+            for (int t0 = t_begin; t0 < t_end && alive;) {
+                const int u = t0 / p.tiles_per_unit;
+                const int t1 = min(t_end, (u + 1) * p.tiles_per_unit);
+                for (int ps = 0; ps < p.npass && alive; ++ps) {
+                    const int rows = min(p.pw, p.cpad - ps * p.pw);
+                    const int nch = (rows + 255) >> 8;
+                    // the previous pass's centroid rows may be overwritten once
+                    // every MMA issued so far has completed
+                    if (b_loads > 0) ptx::mma_commit(&bs->b_empty);
+                    if (!wait_or_abort(&bs->b_full, b_loads & 1, bs, p.dev_err)) {
                         alive = false;
                         break;
                     }
-                    ptx::tc_fence_after();
-                    const int ncols = min(256, p.cpad - 256 * ch);
-                    const uint32_t idesc = ptx::idesc_bf16_f32(128, ncols);
-                    const uint32_t d_tmem = tmem + (uint32_t)slot * 256u;
+                    ++b_loads;
+                    for (int t = t0; t < t1 && alive; ++t, ++it) {
+                        const int s = it % p.stages;
+                        if (!wait_or_abort(&bs->a_full[s], (it / p.stages) & 1, bs, p.dev_err)) {
+                            alive = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                        const uint32_t a_st = a_base + (uint32_t)s * A_STAGE_BYTES;
+                        for (int ch = 0; ch < nch; ++ch, ++item) {
+                            const int slot = item & 1;
+                            if (item >= 2 &&
+                                !wait_or_abort(&bs->tm_empty[slot], ((item >> 1) - 1) & 1, bs, p.dev_err)) {
+                                alive = false;
+                                break;
+                            }
+                            ptx::tc_fence_after();
+                            const int ncols = min(256, rows - 256 * ch);
+                            const uint32_t idesc = ptx::idesc_bf16_f32(128, ncols);
+                            const uint32_t d_tmem = tmem + (uint32_t)slot * 256u;
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const uint32_t koff = (uint32_t)(k & 3) * 32u;
-                        const uint64_t ad = ptx::smem_desc_sw128(a_st + (uint32_t)(k >> 2) * A_PANEL_BYTES + koff);
-                        const uint64_t bd = ptx::smem_desc_sw128(
-                            b_base + (uint32_t)(k >> 2) * (uint32_t)p.cpad * 128u + (uint32_t)ch * 256u * 128u + koff);
-                        ptx::mma_bf16(d_tmem, ad, bd, idesc, k > 0 ? 1u : 0u);
+                            for (int k = 0; k < 8; ++k) {
+                                const uint32_t koff = (uint32_t)(k & 3) * 32u;
+                                const uint64_t ad =
+                                    ptx::smem_desc_sw128(a_st + (uint32_t)(k >> 2) * A_PANEL_BYTES + koff);
+                                const uint64_t bd = ptx::smem_desc_sw128(
+                                    b_base + (uint32_t)(k >> 2) * (uint32_t)p.pw * 128u + (uint32_t)ch * 256u * 128u +
+                                    koff);
+                                ptx::mma_bf16(d_tmem, ad, bd, idesc, k > 0 ? 1u : 0u);
+                            }
+                            ptx::mma_commit(&bs->tm_full[slot]);
+                        }
+                        ptx::mma_commit(&bs->a_empty[s]);
                     }
-                    ptx::mma_commit(&bs->tm_full[slot]);
                 }
-                ptx::mma_commit(&bs->a_empty[s]);
+                t0 = t1;
             }
         }
     } else {
@@ -200,98 +233,125 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int half = (warp - 2) >> 2;
         int item = 0, ntile = 0;
         bool alive = true;
-        for (int t = t_begin; t < t_end && alive; ++t, ++ntile) {
-            const int u = t / p.tiles_per_unit, tl = t % p.tiles_per_unit;
-            // four independent running maxima (columns j mod 4) break the
-            // compare-select dependency chain; merged below
-            float bk[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-            int ak[4] = {0, 0, 0, 0};
-            for (int ch = 0; ch < p.nchunk; ++ch, ++item) {
-                const int slot = item & 1;
-                const bool ok = __all_sync(
-                    0xffffffffu, wait_or_abort(&bs->tm_full[slot], (item >> 1) & 1, bs, p.dev_err));
-                if (!ok) {
-                    alive = false;
-                    break;
-                }
-                ptx::tc_fence_after();
-                const int c0 = 256 * ch;
-                const int nvalid = min(256, p.C - c0);
-                const int ngroups = (nvalid + 31) >> 5;
-                const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)slot * 256u;
-                uint32_t r[4][32];
+        for (int t0 = t_begin; t0 < t_end && alive;) {
+            const int u = t0 / p.tiles_per_unit;
+            const int t1 = min(t_end, (u + 1) * p.tiles_per_unit);
+            for (int ps = 0; ps < p.npass && alive; ++ps) {
+                const int prow = ps * p.pw;
+                const int rows = min(p.pw, p.cpad - prow);
+                const int nch = (rows + 255) >> 8;
+                for (int t = t0; t < t1; ++t, ++ntile) {
+                    const int tl = t - u * p.tiles_per_unit;
+                    // four independent running maxima (columns j mod 4) break the
+                    // compare-select dependency chain; merged below
+                    float bk[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                    int ak[4] = {0, 0, 0, 0};
+                    for (int ch = 0; ch < nch; ++ch, ++item) {
+                        const int slot = item & 1;
+                        const bool ok = __all_sync(
+                            0xffffffffu, wait_or_abort(&bs->tm_full[slot], (item >> 1) & 1, bs, p.dev_err));
+                        if (!ok) {
+                            alive = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                        // chunk columns [c0, c0 + ncols); rows is a multiple of 32 and
+                        // cpad - C < 32, so every chunk holds at least one real column
+                        const int c0 = prow + 256 * ch;
+                        const int nvalid = min(min(256, rows - 256 * ch), p.C - c0);
+                        const int ngroups = (nvalid + 31) >> 5;
+                        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)slot * 256u;
+                        uint32_t r[4][32];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int g = 2 * k + half;
-                    if (g < ngroups) ptx::tmem_ld32(taddr + (uint32_t)(g * 32), r[k]);
-                }
-                ptx::tmem_ld_wait();
+                        for (int k = 0; k < 4; ++k) {
+                            const int g = 2 * k + half;
+                            if (g < ngroups) ptx::tmem_ld32(taddr + (uint32_t)(g * 32), r[k]);
+                        }
+                        ptx::tmem_ld_wait();
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int g = 2 * k + half;
-                    if (g >= ngroups) break;
-                    const int lim = nvalid - g * 32;
-                    const int cb = c0 + g * 32;
-                    if (lim >= 32) {
+                        for (int k = 0; k < 4; ++k) {
+                            const int g = 2 * k + half;
+                            if (g >= ngroups) break;
+                            const int lim = nvalid - g * 32;
+                            const int cb = c0 + g * 32;
+                            if (lim >= 32) {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const float v = __uint_as_float(r[k][j]);
-                            if (v > bk[j & 3]) {
-                                bk[j & 3] = v;
-                                ak[j & 3] = cb + j;
+                                for (int j = 0; j < 32; ++j) {
+                                    const float v = __uint_as_float(r[k][j]);
+                                    if (v > bk[j & 3]) {
+                                        bk[j & 3] = v;
+                                        ak[j & 3] = cb + j;
+                                    }
+                                }
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) {
+                                    const float v = __uint_as_float(r[k][j]);
+                                    if (j < lim && v > bk[j & 3]) {
+                                        bk[j & 3] = v;
+                                        ak[j & 3] = cb + j;
+                                    }
+                                }
                             }
                         }
-                    } else {
+                        ptx::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive(&bs->tm_empty[slot]);
+                    }
+                    if (!alive) break;
+                    // each chain holds its first maximum; (larger value, then lower
+                    // column) over chains and over the pair picks the row's first maximum
+                    float best = bk[0];
+                    int arg = ak[0];
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const float v = __uint_as_float(r[k][j]);
-                            if (j < lim && v > bk[j & 3]) {
-                                bk[j & 3] = v;
-                                ak[j & 3] = cb + j;
+                    for (int k = 1; k < 4; ++k)
+                        if (bk[k] > best || (bk[k] == best && ak[k] < arg)) {
+                            best = bk[k];
+                            arg = ak[k];
+                        }
+                    if (half == 1) {
+                        if (ntile > 0 && !__all_sync(0xffffffffu, wait_or_abort(&bs->pair_free[q], (ntile - 1) & 1,
+                                                                                 bs, p.dev_err))) {
+                            alive = false;
+                            break;
+                        }
+                        bs->xbest[q][lane] = best;
+                        bs->xarg[q][lane] = arg;
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive(&bs->pair_full[q]);
+                    } else {
+                        if (!__all_sync(0xffffffffu,
+                                        wait_or_abort(&bs->pair_full[q], ntile & 1, bs, p.dev_err))) {
+                            alive = false;
+                            break;
+                        }
+                        const float ob = bs->xbest[q][lane];
+                        const int oa = bs->xarg[q][lane];
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive(&bs->pair_free[q]);
+                        if (ob > best || (ob == best && oa < arg)) {
+                            best = ob;
+                            arg = oa;
+                        }
+                        const int row = tl * ASSIGN_TILE + q * 32 + lane;
+                        if (row < p.n) {
+                            const size_t o = (size_t)u * p.n + row;
+                            // earlier passes hold lower columns: they keep ties.
+                            // This thread wrote them itself (same tile row).
+                            if (ps > 0) {
+                                const float pb = p.best[o];
+                                if (!(best > pb)) {
+                                    best = pb;
+                                    arg = p.labels[o];
+                                }
                             }
+                            p.labels[o] = arg;
+                            if (ps + 1 < p.npass) p.best[o] = best;
                         }
                     }
                 }
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&bs->tm_empty[slot]);
             }
-            if (!alive) break;
-            // each chain holds its first maximum; (larger value, then lower
-            // column) over chains and over the pair picks the row's first maximum
-            float best = bk[0];
-            int arg = ak[0];
-#pragma unroll
-            for (int k = 1; k < 4; ++k)
-                if (bk[k] > best || (bk[k] == best && ak[k] < arg)) {
-                    best = bk[k];
-                    arg = ak[k];
-                }
-            if (half == 1) {
-                if (ntile > 0 && !__all_sync(0xffffffffu, wait_or_abort(&bs->pair_free[q], (ntile - 1) & 1, bs, p.dev_err))) {
-                    alive = false;
-                    break;
-                }
-                bs->xbest[q][lane] = best;
-                bs->xarg[q][lane] = arg;
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&bs->pair_full[q]);
-            } else {
-                if (!__all_sync(0xffffffffu, wait_or_abort(&bs->pair_full[q], ntile & 1, bs, p.dev_err))) {
-                    alive = false;
-                    break;
-                }
-                const float ob = bs->xbest[q][lane];
-                const int oa = bs->xarg[q][lane];
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&bs->pair_free[q]);
-                if (ob > best || (ob == best && oa < arg)) {
-                    best = ob;
-                    arg = oa;
-                }
-                const int row = tl * ASSIGN_TILE + q * 32 + lane;
-                if (row < p.n) p.labels[(size_t)u * p.n + row] = arg;
-            }
+            t0 = t1;
         }
     }
 
@@ -338,8 +398,22 @@ bool encode_3d(CUtensorMap* m, const void* base, int rows, int units, int box_ro
 
 }  // namespace
 
+// Centroid rows per pass: all of them up to MAX_ASSIGN_CPAD, else equal passes
+// of at most 512 rows (which leaves room for three key stages).
+void assign_tc_passes(int cpad, int* pw, int* npass) {
+    int np = 1, w = cpad;
+    if (cpad > MAX_ASSIGN_CPAD) {
+        np = ceil_div(cpad, 512);
+        w = round_up(ceil_div(cpad, np), 32);
+    }
+    *pw = w;
+    *npass = np;
+}
+
 size_t assign_tc_smem(int cpad, int* stages_out) {
-    const size_t fixed = (size_t)cpad * 256 + sizeof(Bars) + 1024;
+    int pw = 0, npass = 0;
+    assign_tc_passes(cpad, &pw, &npass);
+    const size_t fixed = (size_t)pw * 256 + sizeof(Bars) + 1024;
     const size_t cap = 232448;
     int stages = 4;
     while (stages > 2 && fixed + (size_t)stages * A_STAGE_BYTES > cap) --stages;
@@ -353,6 +427,9 @@ cudaError_t launch_assign_tc(const ckv_ctx* ctx, const void* K, int n, int C, in
     int stages = 0;
     const size_t smem = assign_tc_smem(cpad, &stages);
     if (smem > 232448 || cpad > ctx->cmax_pad) return cudaErrorInvalidValue;
+    int pw = 0, npass = 0;
+    assign_tc_passes(cpad, &pw, &npass);
+    if (npass > 1 && !ctx->assign_best) return cudaErrorInvalidValue;
     CUtensorMap tmK, tmMu;
     if (!encode_3d(&tmK, K, ctx->cfg.max_len, ctx->cfg.units, ASSIGN_TILE)) return cudaErrorInvalidValue;
     if (!encode_3d(&tmMu, ctx->mu_hat, ctx->cmax_pad, ctx->cfg.units, B_BOX_ROWS))
@@ -361,7 +438,8 @@ cudaError_t launch_assign_tc(const ckv_ctx* ctx, const void* K, int n, int C, in
     a.n = n;
     a.C = C;
     a.cpad = cpad;
-    a.nchunk = ceil_div(cpad, 256);
+    a.pw = pw;
+    a.npass = npass;
     a.tiles_per_unit = ceil_div(n, ASSIGN_TILE);
     a.total_tiles = a.tiles_per_unit * ctx->cfg.units;
     const int grid = a.total_tiles < ctx->num_sms ? a.total_tiles : ctx->num_sms;
@@ -370,6 +448,7 @@ cudaError_t launch_assign_tc(const ckv_ctx* ctx, const void* K, int n, int C, in
     a.sinks = ctx->cfg.sinks;
     a.stages = stages;
     a.labels = labels;
+    a.best = ctx->assign_best;
     a.dev_err = ctx->dev_err;
     cudaError_t e = cudaFuncSetAttribute(assign_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);

@@ -328,12 +328,18 @@ __global__ void __launch_bounds__(G * D) attn_mma_combine_kernel(const float* __
                                                                  int max_slots, float* __restrict__ out) {
     constexpr int PW = G * (D + 2);
     __shared__ float wt[CMB_MAX_SLOTS][G];
+    __shared__ float lw[CMB_MAX_SLOTS][G];
     __shared__ float Ls[G];
     const int u = blockIdx.x, tid = threadIdx.x;
     const int w0 = (u * tpu) / tpw, w1 = (u * tpu + tpu - 1) / tpw;
     const int ns = min(w1 - w0 + 1, CMB_MAX_SLOTS);
     const float* pu = part + (size_t)u * max_slots * PW;
-    for (int e = tid; e < ns * G; e += G * D) wt[e / G][e % G] = pu[(size_t)(e / G) * PW + (e % G) * (D + 2) + D];
+    // every slot's (max, sum) pair at once; the serial part below reads smem only
+    for (int e = tid; e < ns * G; e += G * D) {
+        const float* ms = pu + (size_t)(e / G) * PW + (e % G) * (D + 2) + D;
+        wt[e / G][e % G] = ms[0];
+        lw[e / G][e % G] = ms[1];
+    }
     __syncthreads();
     if (tid < G) {
         float M = -INFINITY;
@@ -341,7 +347,7 @@ __global__ void __launch_bounds__(G * D) attn_mma_combine_kernel(const float* __
         float l = 0.f;
         for (int t = 0; t < ns; ++t) {
             const float f = (wt[t][tid] == -INFINITY) ? 0.f : exp2f(wt[t][tid] - M);
-            l += pu[(size_t)t * PW + tid * (D + 2) + D + 1] * f;
+            l += lw[t][tid] * f;
             wt[t][tid] = f;
         }
         Ls[tid] = l;

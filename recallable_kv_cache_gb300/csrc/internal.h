@@ -55,6 +55,7 @@ struct ckv_ctx {
     float* attn_part;   // [U][max_splits][g * (D + 2)]
     int32_t* attn_cnt;  // [U]
     int32_t* dev_err;   // device error word
+    float* assign_best; // [U][ntok] running arg-max values between assignment passes (large C only)
 };
 
 namespace ckv {

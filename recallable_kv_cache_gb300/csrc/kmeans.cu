@@ -415,11 +415,35 @@ __global__ void __launch_bounds__(256) finalize_kernel(int C, const int32_t* __r
 
 // ---------------------------------------------------------------- incremental
 // One CTA per unit clusters the m newest keys into cp clusters entirely in
-// shared memory: keys as fp32 rows padded to D+1 floats (conflict-free column
-// and row walks), stride seeding, `iters` Lloyd iterations with the same
-// operand precision as the prefill path, then the CSR segment is appended.
+// shared memory: keys in their own dtype (bf16 rows at a 272-byte pitch, fp32
+// rows padded to D+1 floats), stride seeding, `iters` Lloyd iterations with the
+// same operand precision as the prefill path, then the CSR segment is appended.
+// Per iteration:
+//   assignment  bf16 keys: mma.sync m16n8k16 (16 keys x 8 centroid directions
+//               per instruction; exact bf16 products, fp32 sums), arg-max over
+//               the columns of each row in a lane quad; fp32 keys: one thread
+//               per key, fp32 dot products;
+//   order       warp 0 builds the stable cluster order of the keys (counts by
+//               ballot, ranks by match_any), i.e. this iteration's CSR;
+//   update      thread (cluster, channel) sums its channel over the cluster's
+//               keys in token order (compensated), mean of the raw keys; an
+//               empty cluster keeps its centroid.
 constexpr int INCR_THREADS = 512;
 constexpr int INCR_MAX_CP = 16;
+
+template <typename T>
+struct IncrLayout {
+    static constexpr bool BF16 = sizeof(T) == 2;
+    static constexpr int KP = BF16 ? D + 8 : D + 1;  // row pitch in elements
+};
+
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float to_f32(float x) { return x; }
+
+__device__ __forceinline__ uint32_t pack_bf16_exact(float lo, float hi) {
+    // both values are bf16-representable: keep their top halves
+    return (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xffff0000u);
+}
 
 template <typename T>
 __global__ void __launch_bounds__(INCR_THREADS) incr_kernel(const T* __restrict__ K, int max_len, int start,
@@ -427,25 +451,41 @@ __global__ void __launch_bounds__(INCR_THREADS) incr_kernel(const T* __restrict_
                                                             int csr_base, StateRefs st, int32_t* __restrict__ sizes,
                                                             int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
                                                             int ntok) {
-    extern __shared__ __align__(16) float ks[];  // [m][D + 1]
+    using LY = IncrLayout<T>;
+    constexpr int KP = LY::KP;
+    extern __shared__ __align__(16) unsigned char incr_smem[];
+    const int m16 = (m + 15) & ~15;
+    T* ks = reinterpret_cast<T*>(incr_smem);                                   // [m16][KP]
+    int32_t* lab = reinterpret_cast<int32_t*>(ks + (size_t)m16 * KP);          // [m16]
+    int32_t* order = lab + m16;                                                // [m16]
     __shared__ __align__(16) float mu[INCR_MAX_CP][D];
     __shared__ __align__(16) float muh[INCR_MAX_CP][D];
     __shared__ int32_t cnt[INCR_MAX_CP], off[INCR_MAX_CP], run[INCR_MAX_CP];
-    int32_t* lab = reinterpret_cast<int32_t*>(ks + (size_t)m * (D + 1));
-    constexpr int KS = D + 1;
     const int u = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nwarps = INCR_THREADS / 32;
 
-    for (int r = warp; r < m; r += nwarps) {
-        const float4 v = load4(K + ((size_t)u * max_len + start + r) * D, lane);
-        float* dst = ks + (size_t)r * KS + 4 * lane;
-        dst[0] = v.x;
-        dst[1] = v.y;
-        dst[2] = v.z;
-        dst[3] = v.w;
+    // keys (rows past m are zero: they only pad the last 16-row MMA tile)
+    for (int r = warp; r < m16; r += nwarps) {
+        T* dst = ks + (size_t)r * KP;
+        if (r < m) {
+            const T* src = K + ((size_t)u * max_len + start + r) * D;
+            if constexpr (LY::BF16) {
+                reinterpret_cast<uint2*>(dst)[lane] = reinterpret_cast<const uint2*>(src)[lane];
+            } else {
+                const float4 v = reinterpret_cast<const float4*>(src)[lane];
+                dst[4 * lane] = v.x;
+                dst[4 * lane + 1] = v.y;
+                dst[4 * lane + 2] = v.z;
+                dst[4 * lane + 3] = v.w;
+            }
+        } else {
+            for (int c = lane; c < D; c += 32) dst[c] = T(0.f);
+        }
     }
     __syncthreads();
-    for (int e = tid; e < cp * D; e += INCR_THREADS) mu[e / D][e % D] = ks[(size_t)(e / D) * stride * KS + e % D];
+    for (int e = tid; e < cp * D; e += INCR_THREADS)
+        mu[e / D][e % D] = to_f32(ks[(size_t)(e / D) * stride * KP + e % D]);
+    for (int j = tid; j < cp; j += INCR_THREADS) cnt[j] = 0;
     __syncthreads();
 
     for (int it = 0; it < iters; ++it) {
@@ -465,71 +505,142 @@ __global__ void __launch_bounds__(INCR_THREADS) incr_kernel(const T* __restrict_
             muh[j][4 * lane + 3] = x.w;
         }
         __syncthreads();
-        // assignment
-        for (int i = tid; i < m; i += INCR_THREADS) {
-            const float* kr = ks + (size_t)i * KS;
-            float best = -INFINITY;
-            int arg = 0;
-            for (int j = 0; j < cp; ++j) {
-                float dot = 0.f;
-#pragma unroll 8
-                for (int c = 0; c < D; ++c) dot = fmaf(kr[c], muh[j][c], dot);
-                if (dot > best) {
-                    best = dot;
-                    arg = j;
+        // ---- assignment: lab[i] = arg-max_j k_i . muh_j, ties to the lower j
+        if constexpr (LY::BF16) {
+            const int g = lane >> 2, q4 = lane & 3;
+            const int ntiles = (cp + 7) >> 3;  // 8 centroid columns per MMA
+            const uint32_t kbase = static_cast<uint32_t>(__cvta_generic_to_shared(ks));
+            for (int mt = warp; mt < m16 / 16; mt += nwarps) {
+                float best0 = -INFINITY, best1 = -INFINITY;
+                int arg0 = 0, arg1 = 0;
+                for (int nt = 0; nt < ntiles; ++nt) {
+                    const int col = nt * 8 + g;  // centroid of this lane's B column
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const int mi = lane >> 3;
+                        const int row = mt * 16 + (mi & 1) * 8 + (lane & 7);
+                        const uint32_t addr =
+                            kbase + (uint32_t)(row * KP + kk * 16 + (mi >> 1) * 8) * 2u;
+                        uint32_t a0, a1, a2, a3;
+                        asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                                     : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                                     : "r"(addr));
+                        uint32_t b0 = 0u, b1 = 0u;
+                        if (col < cp) {
+                            const float* mh = muh[col] + kk * 16 + 2 * q4;
+                            b0 = pack_bf16_exact(mh[0], mh[1]);
+                            b1 = pack_bf16_exact(mh[8], mh[9]);
+                        }
+                        asm volatile(
+                            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+                            "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                            : "+f"(acc[0]), "+f"(acc[1]), "+f"(acc[2]), "+f"(acc[3])
+                            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+                    }
+                    // this lane holds rows g (acc 0, 1) and g + 8 (acc 2, 3),
+                    // columns nt*8 + 2*q4 and + 1, visited in increasing order
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int cc = nt * 8 + 2 * q4 + e;
+                        if (cc < cp) {
+                            if (acc[e] > best0) { best0 = acc[e]; arg0 = cc; }
+                            if (acc[2 + e] > best1) { best1 = acc[2 + e]; arg1 = cc; }
+                        }
+                    }
+                }
+                // quad reduction: larger value, then lower column
+#pragma unroll
+                for (int o = 1; o <= 2; o <<= 1) {
+                    const float ob0 = __shfl_xor_sync(FULL, best0, o), ob1 = __shfl_xor_sync(FULL, best1, o);
+                    const int oa0 = __shfl_xor_sync(FULL, arg0, o), oa1 = __shfl_xor_sync(FULL, arg1, o);
+                    if (ob0 > best0 || (ob0 == best0 && oa0 < arg0)) { best0 = ob0; arg0 = oa0; }
+                    if (ob1 > best1 || (ob1 == best1 && oa1 < arg1)) { best1 = ob1; arg1 = oa1; }
+                }
+                if (q4 == 0) {
+                    lab[mt * 16 + g] = arg0;
+                    lab[mt * 16 + g + 8] = arg1;
                 }
             }
-            lab[i] = arg;
+        } else {
+            for (int i = tid; i < m; i += INCR_THREADS) {
+                const T* kr = ks + (size_t)i * KP;
+                float best = -INFINITY;
+                int arg = 0;
+                for (int j = 0; j < cp; ++j) {
+                    float dot = 0.f;
+#pragma unroll 8
+                    for (int c = 0; c < D; ++c) dot = fmaf(to_f32(kr[c]), muh[j][c], dot);
+                    if (dot > best) {
+                        best = dot;
+                        arg = j;
+                    }
+                }
+                lab[i] = arg;
+            }
         }
         __syncthreads();
-        // update: thread (j, c) sums its channel over the cluster in token order
+        // ---- stable cluster order of the keys (warp 0)
+        if (warp == 0) {
+            int my_cnt = 0;  // lane j < cp: size of cluster j
+            for (int b = 0; b < m; b += 32) {
+                const int l = (b + lane < m) ? lab[b + lane] : -1;
+                for (int j = 0; j < cp; ++j) {
+                    const int n = __popc(__ballot_sync(FULL, l == j));
+                    if (lane == j) my_cnt += n;
+                }
+            }
+            int incl = my_cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(FULL, incl, o);
+                if (lane >= o) incl += t;
+            }
+            if (lane < cp) {
+                cnt[lane] = my_cnt;
+                off[lane] = incl - my_cnt;
+                run[lane] = 0;
+            }
+            __syncwarp();
+            for (int b = 0; b < m; b += 32) {
+                const int i = b + lane;
+                const int l = i < m ? lab[i] : -1;
+                const unsigned peers = __match_any_sync(FULL, l);
+                const int rank = __popc(peers & ((1u << lane) - 1u));
+                if (i < m) order[off[l] + run[l] + rank] = i;
+                __syncwarp();
+                if (i < m && rank == 0) run[l] += __popc(peers);
+                __syncwarp();
+            }
+        }
+        __syncthreads();
+        // ---- update: thread (j, c) over cluster j's keys in token order
         for (int e = tid; e < cp * D; e += INCR_THREADS) {
             const int j = e / D, c = e % D;
-            Kahan a;
-            int count = 0;
-            for (int i = 0; i < m; ++i)
-                if (lab[i] == j) {
-                    a.add(ks[(size_t)i * KS + c]);
-                    ++count;
-                }
-            if (count > 0) mu[j][c] = a.value() / (float)count;
-            if (c == 0) cnt[j] = count;
+            const int n = cnt[j], o0 = off[j];
+            if (n > 0) {
+                Kahan a;
+                for (int p = 0; p < n; ++p) a.add(to_f32(ks[(size_t)order[o0 + p] * KP + c]));
+                mu[j][c] = a.value() / (float)n;
+            }
         }
-        __syncthreads();
-    }
-    if (iters == 0) {
-        for (int j = tid; j < cp; j += INCR_THREADS) cnt[j] = 0;
         __syncthreads();
     }
 
-    // CSR segment: sizes, offsets, stable permutation (warp 0)
-    if (tid == 0) {
-        int acc = 0;
-        for (int j = 0; j < cp; ++j) {
-            off[j] = acc;
-            run[j] = 0;
-            acc += cnt[j];
-        }
-    }
+    // CSR segment of the last assignment: sizes, offsets, stable permutation
+    if (iters > 0)
+        for (int p = tid; p < m; p += INCR_THREADS) perm[(size_t)u * ntok + csr_base + p] = start + order[p];
+    else if (tid == 0)
+        for (int j = 0; j < cp; ++j) off[j] = 0;
     __syncthreads();
-    if (warp == 0) {
-        for (int b = 0; b < m; b += 32) {
-            const int i = b + lane;
-            const int l = i < m ? lab[i] : -1;
-            const unsigned peers = __match_any_sync(FULL, l);
-            const int rank = __popc(peers & ((1u << lane) - 1u));
-            if (i < m) perm[(size_t)u * ntok + csr_base + off[l] + run[l] + rank] = start + i;
-            __syncwarp();
-            if (i < m && rank == 0) run[l] += __popc(peers);
-            __syncwarp();
-        }
-    }
+    if (iters == 0)  // no assignment: every key in cluster 0 (the seeds are the centroids)
+        for (int p = tid; p < m; p += INCR_THREADS) perm[(size_t)u * ntok + csr_base + p] = start + p;
     for (int j = warp; j < cp; j += nwarps) {
         const float4 v = make_float4(mu[j][4 * lane], mu[j][4 * lane + 1], mu[j][4 * lane + 2], mu[j][4 * lane + 3]);
         st.store(u, C_old + j, v, lane);
         if (lane == 0) {
-            sizes[(size_t)u * st.cmax + C_old + j] = cnt[j];
-            offsets[(size_t)u * (st.cmax + 1) + C_old + j] = csr_base + off[j];
+            sizes[(size_t)u * st.cmax + C_old + j] = iters > 0 ? cnt[j] : (j == 0 ? m : 0);
+            offsets[(size_t)u * (st.cmax + 1) + C_old + j] = csr_base + (iters > 0 ? off[j] : (j == 0 ? 0 : m));
         }
     }
     if (tid == 0) offsets[(size_t)u * (st.cmax + 1) + C_old + cp] = csr_base + m;
@@ -598,12 +709,16 @@ cudaError_t launch_update(const ckv_ctx* ctx, const void* K, int n, int C, const
     return update_t(ctx, (const float*)K, n, C, labels, s);
 }
 
-size_t incremental_smem(int m) { return (size_t)m * (D + 1) * sizeof(float) + (size_t)m * sizeof(int32_t); }
+size_t incremental_smem(int m, bool bf16) {
+    const size_t m16 = (size_t)((m + 15) & ~15);
+    const size_t row = bf16 ? (size_t)IncrLayout<__nv_bfloat16>::KP * 2 : (size_t)IncrLayout<float>::KP * 4;
+    return m16 * row + 2 * m16 * sizeof(int32_t);
+}
 
 cudaError_t launch_incremental(const ckv_ctx* ctx, const void* K, int start, int m, int c_plus, int C_old,
                                int csr_base, cudaStream_t s) {
     if (c_plus > INCR_MAX_CP) return cudaErrorInvalidValue;
-    const size_t smem = incremental_smem(m);
+    const size_t smem = incremental_smem(m, ctx->cfg.kv_dtype == CKV_BF16);
     const int stride = (m / c_plus) < ctx->cfg.ratio ? (m / c_plus) : ctx->cfg.ratio;
     cudaError_t e;
     if (ctx->cfg.kv_dtype == CKV_BF16) {

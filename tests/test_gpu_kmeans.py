@@ -22,7 +22,9 @@ def operand(w):
 
 
 # (workload, units, L, C): ragged token tails (n % 128 != 0) and centroid
-# counts that need 1, 2 and 3 TMEM column chunks (C <= 256, <= 512, > 512)
+# counts that need 1, 2 and 3 TMEM column chunks (C <= 256, <= 512, > 512),
+# and counts above 640 that the kernel splits into passes over the keys
+# (700: two passes of 352 rows; 1638, the 128k workload's C: four of 416)
 ASSIGN_CASES = [
     ("layer_32k", 2, 16 + 1000, 13),
     ("layer_32k", 2, 16 + 3000, 300),
@@ -30,6 +32,8 @@ ASSIGN_CASES = [
     ("layer_32k", 3, 16 + 129, 1),
     ("tiny_2k", 1, 2048, 25),
     ("tiny_2k", 2, 16 + 700, 41),
+    ("layer_32k", 2, 16 + 2600, 700),
+    ("long_128k", 1, 16 + 4000, 1638),
 ]
 
 
@@ -65,6 +69,33 @@ def test_assign_lockstep(wname, U, L, C):
         if U > 1:
             assert (got[1, 40 - 16:45 - 16] == 0).all()
     ctx.close()
+
+
+@pytest.mark.parametrize("C,dups", [(400, [(5, 300)]), (700, [(10, 600), (3, 200), (400, 690)])])
+def test_assign_duplicate_centroids_tie_to_lower(C, dups):
+    """Two centroids with the same direction give bit-identical dots, so every
+    key nearest to them must take the lower index, whether the copies sit in
+    one TMEM chunk, two chunks, or two passes over the keys."""
+    w = workload("layer_32k", units=2, L=16 + 3000, decode_steps=0, C=C, n_centres=C)
+    K, _ = synth.make_kv(w)
+    n = w.L - 16
+    ctx = make_ctx(2, w.g, w.max_len, C, 64, w.dtype, iters=1)
+    mu32 = np.stack([ck.seed_centroids(to64(K[u, 16:w.L]), C) for u in range(2)]).astype(np.float32)
+    for lo, hi in dups:
+        mu32[:, hi] = 2.0 * mu32[:, lo]   # same direction, other norm
+    ctx.import_clusters(C, 0, torch.from_numpy(mu32).cuda())
+    labels = torch.empty(2, n, dtype=torch.int32, device="cuda")
+    ctx.kmeans_assign(K.cuda().contiguous(), w.L, labels)
+    got = labels.cpu().numpy()
+    ctx.close()
+    for u in range(2):
+        mu_hat, _ = ck.normalize_centroids(mu32[u].astype(np.float64), "bf16")
+        lab_o = ck.assign(to64(K[u, 16:w.L]), mu_hat)
+        check_assignment(to64(K[u, 16:w.L]), mu32[u].astype(np.float64), got[u], "bf16")
+        for lo, hi in dups:
+            assert np.array_equal(mu_hat[lo], mu_hat[hi])
+            assert (lab_o == lo).any(), "the duplicated centroid should attract keys"
+            assert not (got[u] == hi).any(), f"a key took the higher duplicate {hi}"
 
 
 @pytest.mark.parametrize("wname,U,L,C", ASSIGN_CASES[:5])
