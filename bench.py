@@ -257,6 +257,8 @@ def run_ours(args, w, rank, world, device):
     res["attn_bytes_per_launch"] = statistics.mean(decode_bytes(w, t, C_at[t])[0] for t in sampled)
     res["decode_bytes_per_step"] = sum(decode_bytes(w, t, C_at[t])[1] for t in range(T)) / T
     res["assign_ms"] = time_assign(ctx, w, K)
+    res["recall"] = selection_recall(ctx, w, K, Q)
+    res["full_kv"] = full_kv_attention(w, K, V, Q)
     res["w"] = w
     res["ctx"] = ctx
     res["tensors"] = (K, V, Q)
@@ -281,6 +283,66 @@ def time_assign(ctx, w, K, reps=5):
     a1.record()
     torch.cuda.synchronize()
     return a0.elapsed_time(a1) / reps
+
+
+def selection_recall(ctx, w, K, Q, units=(0, 97, 201), queries=(0, 1, 2)):
+    """Recall of the cluster selection against the exact top-B tokens by
+    sum_h q_h . k (a measurement, not part of the path): token recall
+    |S n TopB| / B and attention-mass recall sum_S a / sum_TopB a, a = the full
+    softmax over the clustered prompt tokens averaged over the g heads.  The
+    selection is the library's (prefill clusters, decode step 0 state)."""
+    idx = torch.empty(w.units, w.B, dtype=torch.int32, device="cuda")
+    cnt = torch.empty(w.units, dtype=torch.int32, device="cuda")
+    tok, mass = [], []
+    for qi in queries:
+        q = Q[qi]
+        ctx.select(q, w.B, idx, cnt)
+        torch.cuda.synchronize()
+        for u in units:
+            keys = K[u, w.sinks:w.L].float()
+            qu = q[u].float()                                        # [g, d]
+            logits = qu @ keys.T / (w.d ** 0.5)                      # [g, n]
+            a = torch.softmax(logits, dim=1).mean(0)                 # [n]
+            top = torch.topk((qu.sum(0) @ keys.T), w.B).indices
+            sel = idx[u, :int(cnt[u])].long() - w.sinks
+            inter = torch.isin(sel, top).sum().item()
+            tok.append(inter / w.B)
+            mass.append((a[sel].sum() / a[top].sum()).item())
+    return {"token": statistics.mean(tok), "attention_mass": statistics.mean(mass),
+            "sample": f"{len(units)} units x {len(queries)} queries, prefill clusters, B={w.B}"}
+
+
+def full_kv_attention(w, K, V, Q, reps=5):
+    """Comparator: the same attention kernel over every token (B = L - sinks,
+    all prompt tokens selected) for all units, timed alone with CUDA events."""
+    from recallable_kv_cache_gb300 import ckv
+    n = w.L - w.sinks
+    fctx = ckv.Context(units=w.units, g=w.g, max_len=w.L, max_clusters=1, max_budget=n, iters=1,
+                       m=w.m, c_plus=w.c_plus)
+    idx = torch.arange(w.sinks, w.L, dtype=torch.int32, device="cuda").expand(w.units, n).contiguous()
+    cnt = torch.full((w.units,), n, dtype=torch.int32, device="cuda")
+    out = torch.empty(w.units, w.g, w.d, dtype=torch.float32, device="cuda")
+    # one cluster holding the whole prompt, so that every prompt token counts as
+    # clustered and none as pending
+    mu = torch.zeros(w.units, 1, w.d, dtype=torch.float32, device="cuda")
+    sizes = torch.full((w.units, 1), n, dtype=torch.int32, device="cuda")
+    offs = torch.tensor([0, n], dtype=torch.int32, device="cuda").expand(w.units, 2).contiguous()
+    fctx.import_clusters(1, w.L, mu, sizes, offs, idx)
+    Kp, Vp = K[:, :w.L].contiguous(), V[:, :w.L].contiguous()
+    for _ in range(3):
+        fctx.sparse_decode_attn(Q[0], Kp, Vp, idx, cnt, n, w.L, out)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for r in range(reps):
+        fctx.sparse_decode_attn(Q[r + 1], Kp, Vp, idx, cnt, n, w.L, out)
+    e1.record()
+    torch.cuda.synchronize()
+    fctx.close()
+    us = 1000.0 * e0.elapsed_time(e1) / reps
+    byts = w.units * (w.L * 2 * w.d * 2 + n * 4)
+    return {"attention_us": us, "gbs": byts / (us / 1e6) / 1e9,
+            "what": "attention over all L tokens of every unit with the same kernel (idx = every prompt token)"}
 
 
 def run_e2e(ctx, w, K, V, Q):
@@ -472,6 +534,8 @@ def main():
                             "peak": meas.get("bf16_tflops", 1900.0), "unit": "TFLOP/s",
                             "frac": assign_flops / (r["assign_ms"] / 1000.0) / 1e12 / meas.get("bf16_tflops", 1900.0),
                             "launch_us": 1000.0 * r["assign_ms"], "peak_kind": peak_kind + " (burst: timed alone)"},
+        "recall": r["recall"],
+        "full_kv": dict(r["full_kv"], decode_speedup=r["full_kv"]["attention_us"] / (1000.0 * decode_ms / T)),
         "phase_ms": {"prefill_clustering": prefill_ms, "decode_loop": decode_ms},
         "per_launch_us": {"select": 1000.0 * r["select_ms"], "attention": 1000.0 * r["attn_ms"]},
         "gpu_launches": r["launches"], "clocks": r["clocks"],

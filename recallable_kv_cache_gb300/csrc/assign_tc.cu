@@ -21,10 +21,10 @@
 //   warp 1     TMEM owner and MMA issuer: per tile and per column chunk of at
 //              most 256 centroids, 8 x tcgen05.mma (K = 16 each) into one of
 //              two 256-column TMEM slots;
-//   warps 2-9  epilogue: tcgen05.ld of the fp32 dots (one TMEM lane = one
-//              token; two warps per lane quarter split the 32-column groups),
+//   warps 2-17 epilogue: tcgen05.ld of the fp32 dots (one TMEM lane = one
+//              token; four warps per lane quarter split the 32-column groups),
 //              running arg-max in increasing centroid order with a strict '>'
-//              (ties keep the lower index), pair merge, label store.
+//              (ties keep the lower index), merge of the four, label store.
 // All mbarrier waits are bounded; a timeout sets the device error word and
 // every role leaves its loop.
 #include <cuda.h>
@@ -42,7 +42,10 @@ namespace {
 constexpr int A_STAGE_BYTES = ASSIGN_TILE * D * 2;  // 32 KB: two 64-column panels
 constexpr int A_PANEL_BYTES = ASSIGN_TILE * 128;    // 16 KB
 constexpr int B_BOX_ROWS = 32;
-constexpr int THREADS = 320;  // producer, MMA issuer, 8 epilogue warps
+constexpr int EPI_PER_Q = 4;                    // epilogue warps per TMEM lane quarter
+constexpr int EPI_WARPS = 4 * EPI_PER_Q;
+constexpr int THREADS = 64 + 32 * EPI_WARPS;     // producer, MMA issuer, epilogue warps
+constexpr int GROUPS_PER_WARP = 8 / EPI_PER_Q;   // 32-column groups of a 256-column chunk
 
 struct AssignArgs {
     int n;              // clustered tokens per unit
@@ -67,10 +70,10 @@ struct __align__(8) Bars {
     uint64_t b_empty;
     uint64_t tm_full[2];
     uint64_t tm_empty[2];
-    uint64_t pair_full[4];   // per TMEM lane quarter: second-half partials written
-    uint64_t pair_free[4];   // ... and consumed
-    float xbest[4][32];
-    int xarg[4][32];
+    uint64_t part_full[4];   // per TMEM lane quarter: the other warps' partials written
+    uint64_t part_free[4];   // ... and consumed
+    float xbest[4][EPI_PER_Q - 1][32];
+    int xarg[4][EPI_PER_Q - 1][32];
     uint32_t tmem_base;
     int abort;
 };
@@ -106,11 +109,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         ptx::mbar_init(&bs->b_empty, 1);
         for (int s = 0; s < 2; ++s) {
             ptx::mbar_init(&bs->tm_full[s], 1);
-            ptx::mbar_init(&bs->tm_empty[s], 8);
+            ptx::mbar_init(&bs->tm_empty[s], EPI_WARPS);
         }
         for (int qq = 0; qq < 4; ++qq) {
-            ptx::mbar_init(&bs->pair_full[qq], 1);
-            ptx::mbar_init(&bs->pair_free[qq], 1);
+            ptx::mbar_init(&bs->part_full[qq], EPI_PER_Q - 1);
+            ptx::mbar_init(&bs->part_free[qq], 1);
         }
         bs->abort = 0;
         ptx::fence_barrier_init();
@@ -224,13 +227,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        // warps 2..9: two per TMEM lane quarter (warp % 4); the first of a pair
-        // takes the even 32-column groups of every chunk, the second the odd
-        // ones.  Each warp issues all its TMEM loads of a chunk (at most four
-        // groups) before one wait.  Per row the pair's partial arg-maxes are
-        // merged through shared memory; ties keep the lower column.
+        // EPI_PER_Q warps per TMEM lane quarter (warp % 4); warp `sub` of a
+        // quarter takes the 32-column groups sub, sub + EPI_PER_Q, ... of every
+        // chunk and issues all its TMEM loads of a chunk before one wait.  Per
+        // row the partial arg-maxes are merged through shared memory by the
+        // quarter's first warp; ties keep the lower column.
         const int q = warp & 3;
-        const int half = (warp - 2) >> 2;
+        const int sub = (warp - 2) >> 2;  // rank among the quarter's epilogue warps
         int item = 0, ntile = 0;
         bool alive = true;
         for (int t0 = t_begin; t0 < t_end && alive;) {
@@ -261,16 +264,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const int nvalid = min(min(256, rows - 256 * ch), p.C - c0);
                         const int ngroups = (nvalid + 31) >> 5;
                         const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)slot * 256u;
-                        uint32_t r[4][32];
+                        uint32_t r[GROUPS_PER_WARP][32];
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const int g = 2 * k + half;
+                        for (int k = 0; k < GROUPS_PER_WARP; ++k) {
+                            const int g = EPI_PER_Q * k + sub;
                             if (g < ngroups) ptx::tmem_ld32(taddr + (uint32_t)(g * 32), r[k]);
                         }
                         ptx::tmem_ld_wait();
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const int g = 2 * k + half;
+                        for (int k = 0; k < GROUPS_PER_WARP; ++k) {
+                            const int g = EPI_PER_Q * k + sub;
                             if (g >= ngroups) break;
                             const int lim = nvalid - g * 32;
                             const int cb = c0 + g * 32;
@@ -309,30 +312,37 @@ __global__ void __launch_bounds__(THREADS, 1)
                             best = bk[k];
                             arg = ak[k];
                         }
-                    if (half == 1) {
-                        if (ntile > 0 && !__all_sync(0xffffffffu, wait_or_abort(&bs->pair_free[q], (ntile - 1) & 1,
+                    if (sub > 0) {
+                        if (ntile > 0 && !__all_sync(0xffffffffu, wait_or_abort(&bs->part_free[q], (ntile - 1) & 1,
                                                                                  bs, p.dev_err))) {
                             alive = false;
                             break;
                         }
-                        bs->xbest[q][lane] = best;
-                        bs->xarg[q][lane] = arg;
+                        bs->xbest[q][sub - 1][lane] = best;
+                        bs->xarg[q][sub - 1][lane] = arg;
                         __syncwarp();
-                        if (lane == 0) ptx::mbar_arrive(&bs->pair_full[q]);
+                        if (lane == 0) ptx::mbar_arrive(&bs->part_full[q]);
                     } else {
                         if (!__all_sync(0xffffffffu,
-                                        wait_or_abort(&bs->pair_full[q], ntile & 1, bs, p.dev_err))) {
+                                        wait_or_abort(&bs->part_full[q], ntile & 1, bs, p.dev_err))) {
                             alive = false;
                             break;
                         }
-                        const float ob = bs->xbest[q][lane];
-                        const int oa = bs->xarg[q][lane];
-                        __syncwarp();
-                        if (lane == 0) ptx::mbar_arrive(&bs->pair_free[q]);
-                        if (ob > best || (ob == best && oa < arg)) {
-                            best = ob;
-                            arg = oa;
+                        float ob[EPI_PER_Q - 1];
+                        int oa[EPI_PER_Q - 1];
+#pragma unroll
+                        for (int w = 0; w < EPI_PER_Q - 1; ++w) {
+                            ob[w] = bs->xbest[q][w][lane];
+                            oa[w] = bs->xarg[q][w][lane];
                         }
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive(&bs->part_free[q]);
+#pragma unroll
+                        for (int w = 0; w < EPI_PER_Q - 1; ++w)
+                            if (ob[w] > best || (ob[w] == best && oa[w] < arg)) {
+                                best = ob[w];
+                                arg = oa[w];
+                            }
                         const int row = tl * ASSIGN_TILE + q * 32 + lane;
                         if (row < p.n) {
                             const size_t o = (size_t)u * p.n + row;
