@@ -106,6 +106,8 @@ template <int G>
 __global__ void __launch_bounds__(MW * 32, 1) attn_mma_kernel(const MmaArgs a) {
     constexpr int PW = G * (D + 2);
     extern __shared__ __align__(128) unsigned char mma_smem[];
+    ptx::grid_dependency_wait();  // idx and count come from the selection kernel
+    ptx::allow_dependent_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gw = blockIdx.x * MW + warp;
     const int t_begin = gw * a.tpw;
@@ -371,7 +373,8 @@ __global__ void __launch_bounds__(G * D) attn_mma_combine_kernel(const float* __
 template <int G>
 cudaError_t launch_mma_t(const void* q, const void* K, const void* V, const int32_t* idx, const int32_t* count,
                          int units, int max_len, int sinks, int clustered_end, int cur_len, int B, float* out,
-                         float* part, int max_slots, int32_t* dev_err, int num_sms, cudaStream_t st) {
+                         float* part, int32_t* counters, int max_slots, int32_t* dev_err, int num_sms,
+                         cudaStream_t st) {
     MmaArgs a;
     a.q = static_cast<const __nv_bfloat16*>(q);
     a.K = static_cast<const __nv_bfloat16*>(K);
@@ -400,8 +403,7 @@ cudaError_t launch_mma_t(const void* q, const void* K, const void* V, const int3
     auto kern = attn_mma_kernel<G>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, MW * 32, smem, st>>>(a);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_dependent(kern, dim3(grid), dim3(MW * 32), smem, st, a)) != cudaSuccess) return e;
     attn_mma_combine_kernel<G><<<units, G * D, 0, st>>>(part, a.tpu, a.tpw, max_slots, out);
     return cudaGetLastError();
 }
@@ -412,14 +414,18 @@ int attention_mma_rows_per_tile() { return TR; }
 
 cudaError_t launch_attention_mma(const void* q, const void* K, const void* V, const int32_t* idx,
                                  const int32_t* count, int units, int g, int max_len, int sinks, int clustered_end,
-                                 int cur_len, int B, float* out, float* part, int max_slots, int32_t* dev_err,
-                                 int num_sms, cudaStream_t s) {
+                                 int cur_len, int B, float* out, float* part, int32_t* counters, int max_slots,
+                                 int32_t* dev_err, int num_sms, cudaStream_t s) {
+#define CKV_MMA(G)                                                                                            \
+    return launch_mma_t<G>(q, K, V, idx, count, units, max_len, sinks, clustered_end, cur_len, B, out, part, \
+                           counters, max_slots, dev_err, num_sms, s)
     switch (g) {
-        case 1: return launch_mma_t<1>(q, K, V, idx, count, units, max_len, sinks, clustered_end, cur_len, B, out, part, max_slots, dev_err, num_sms, s);
-        case 2: return launch_mma_t<2>(q, K, V, idx, count, units, max_len, sinks, clustered_end, cur_len, B, out, part, max_slots, dev_err, num_sms, s);
-        case 4: return launch_mma_t<4>(q, K, V, idx, count, units, max_len, sinks, clustered_end, cur_len, B, out, part, max_slots, dev_err, num_sms, s);
-        case 8: return launch_mma_t<8>(q, K, V, idx, count, units, max_len, sinks, clustered_end, cur_len, B, out, part, max_slots, dev_err, num_sms, s);
+        case 1: CKV_MMA(1);
+        case 2: CKV_MMA(2);
+        case 4: CKV_MMA(4);
+        case 8: CKV_MMA(8);
     }
+#undef CKV_MMA
     return cudaErrorInvalidValue;
 }
 

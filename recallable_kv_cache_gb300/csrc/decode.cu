@@ -103,6 +103,30 @@ __global__ void __launch_bounds__(256) score_kernel(const T* __restrict__ q,
 // ============================================================================
 // selection: one CTA per unit
 // ============================================================================
+// ascending bitonic sort of one 64-bit key per lane
+__device__ __forceinline__ uint64_t warp_sort32(uint64_t x, int lane) {
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1)
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const uint64_t p = __shfl_xor_sync(FULL, x, j);
+            const bool keep_min = ((lane & j) == 0) == ((lane & k) == 0);
+            x = keep_min ? (x < p ? x : p) : (x < p ? p : x);
+        }
+    return x;
+}
+// a, b ascending across the lanes: the 32 smallest of a and b, ascending
+__device__ __forceinline__ uint64_t warp_merge32(uint64_t a, uint64_t b, int lane) {
+    const uint64_t br = __shfl_sync(FULL, b, 31 - lane);
+    uint64_t x = a < br ? a : br;  // bitonic, holds the 32 smallest
+#pragma unroll
+    for (int j = 16; j > 0; j >>= 1) {
+        const uint64_t p = __shfl_xor_sync(FULL, x, j);
+        x = (lane & j) ? (x < p ? p : x) : (x < p ? x : p);
+    }
+    return x;
+}
+
 __device__ __forceinline__ uint64_t rank_key(float s, int c) {
     if (s == 0.f) s = 0.f;  // -0 ranks like +0
     const uint32_t b = __float_as_uint(s);
@@ -136,6 +160,8 @@ __global__ void __launch_bounds__(1024, 1) sel_kernel(
     __shared__ int32_t s_tot;
     const int u = blockIdx.x, tid = threadIdx.x, NT = blockDim.x;
     const int lane = tid & 31, warp = tid >> 5, nwarps = NT >> 5;
+    ptx::grid_dependency_wait();    // q, the cluster state and idx may come from the previous kernel
+    ptx::allow_dependent_launch();
 
     // ---- 1. sizes / offsets (registers first, shared memory after the scores)
     int szr[E], ofr[E];
@@ -202,7 +228,65 @@ __global__ void __launch_bounds__(1024, 1) sel_kernel(
     }
     __syncthreads();
 
-    // ---- 3. exact candidate pre-filter: a size-weighted histogram over the
+    // ---- 3. fast path: the 32 highest-ranked clusters.  Warp w sorts the E
+    // lists of 32 keys it owns (in registers; sk keeps its order) and merges
+    // them into its 32 smallest keys; warp 0 merges the warps' lists in four
+    // independent chains.  If those 32 clusters hold min(B, total) tokens, the
+    // selection is a prefix of them and the rest of the ranking is not needed.
+    __shared__ int s_fast, s_nsel, s_total;
+    uint64_t* part = reinterpret_cast<uint64_t*>(start);  // [nwarps][32] (start/cl reused)
+    {
+        uint64_t top = warp_sort32(sk[32 * warp + lane], lane);
+#pragma unroll
+        for (int e = 1; e < E; ++e)
+            top = warp_merge32(top, warp_sort32(sk[32 * (warp + e * nwarps) + lane], lane), lane);
+        part[32 * warp + lane] = top;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int tot = 0;  // clustered tokens: the sum of all sizes
+        for (int c = lane; c < C; c += 32) tot += szc[c];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(FULL, tot, o);
+        uint64_t ch[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) ch[k] = k < nwarps ? part[32 * k + lane] : ~0ull;
+        for (int l = 4; l < nwarps; l += 4)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (l + k < nwarps) ch[k] = warp_merge32(ch[k], part[32 * (l + k) + lane], lane);
+        const uint64_t top = warp_merge32(warp_merge32(ch[0], ch[1], lane), warp_merge32(ch[2], ch[3], lane), lane);
+        const int target = tot < B ? tot : B;
+        const int c = (int)(uint32_t)top;
+        const int sz = (top != ~0ull && c < C) ? szc[c] : 0;
+        int incl = sz;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(FULL, incl, o);
+            if (lane >= o) incl += t;
+        }
+        // ranks needed: the first rank whose inclusive prefix reaches the target
+        const unsigned reach = __ballot_sync(FULL, incl >= target);
+        const bool fast = target == 0 || reach != 0u;
+        const int nsel = target == 0 ? 0 : (reach ? __ffs(reach) : 0);
+        __syncwarp();  // every lane has read part before start / cl (same storage) are written
+        if (fast && lane < nsel) {
+            start[lane] = incl - sz;
+            cl[lane] = c;
+        }
+        if (lane == 0) {
+            s_fast = fast;
+            s_nsel = nsel;
+            s_total = tot;
+        }
+    }
+    __syncthreads();
+    int nsorted;
+    const int total = s_total;
+    if (s_fast) {
+        nsorted = s_nsel;
+    } else {
+    // ---- 3'. exact candidate pre-filter: a size-weighted histogram over the
     // top 12 bits of the keys (ascending key = descending score) gives the
     // first bin at which the cumulative size reaches min(B, total).  Clusters
     // in earlier bins rank before every cluster of that bin, clusters in later
@@ -211,7 +295,7 @@ __global__ void __launch_bounds__(1024, 1) sel_kernel(
     constexpr int HBITS = 12, NBIN = 1 << HBITS;
     int32_t* hist = offc + N;                                 // [NBIN]
     uint64_t* cand = reinterpret_cast<uint64_t*>(start);      // [<= NT] (start/cl reused)
-    __shared__ int32_t s_bstar, s_total, s_M;
+    __shared__ int32_t s_bstar, s_M;
     for (int i = tid; i < NBIN; i += NT) hist[i] = 0;
     if (tid == 0) s_M = 0;
     __syncthreads();
@@ -258,7 +342,7 @@ __global__ void __launch_bounds__(1024, 1) sel_kernel(
         }
     }
     __syncthreads();
-    const int total = s_total, bstar = s_bstar;
+    const int bstar = s_bstar;
     // every cluster needs ranking when the budget covers all tokens
     const bool take_all = total <= B;
     if (!take_all) {
@@ -278,7 +362,6 @@ __global__ void __launch_bounds__(1024, 1) sel_kernel(
     __syncthreads();
     const int M = s_M;
     const bool small = !take_all && M <= NT;
-    int nsorted;
     if (small && M <= 32) {
         // ---- 3a. up to 32 candidates: one warp, shuffles only
         if (warp == 0) {
@@ -404,6 +487,8 @@ __global__ void __launch_bounds__(1024, 1) sel_kernel(
         base += seg_total;
         __syncthreads();
     }
+
+    }  // histogram path
 
     // ---- 5. cut at the budget and compact the token ids
     const int cnt = total < B ? total : B;
@@ -945,10 +1030,10 @@ cudaError_t launch_sel_t(const ckv_ctx* ctx, const void* q, const float* scores,
     auto kern = sel_kernel<T, G, E, FS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<ctx->cfg.units, N / E, smem, s>>>((const T*)q, (const T*)ctx->mu_s, ctx->cmax, scores, stride, C, N,
-                                             ctx->sizes, ctx->offsets, ctx->perm, ctx->ntok, B, idx, count,
-                                             ctx->dev_err);
-    return cudaGetLastError();
+    return launch_dependent(kern, dim3(ctx->cfg.units), dim3(N / E), smem, s, (const T*)q, (const T*)ctx->mu_s,
+                            ctx->cmax, scores, stride, C, N, (const int32_t*)ctx->sizes,
+                            (const int32_t*)ctx->offsets, (const int32_t*)ctx->perm, ctx->ntok, B, idx, count,
+                            ctx->dev_err);
 }
 
 template <typename T, int E, bool FS>
@@ -1009,7 +1094,7 @@ cudaError_t launch_attention(const void* q, const void* K, const void* V, const 
     if (kv_dtype == CKV_BF16) {
         // bf16 K/V: tensor-core kernel (attn_mma.cu); fp32 K/V: CUDA-core kernel below
         return launch_attention_mma(q, K, V, idx, count, units, g, max_len, sinks, clustered_end, cur_len, B,
-                                    out, part, max_splits, dev_err, num_sms, s);
+                                    out, part, counters, max_splits, dev_err, num_sms, s);
     } else {
         switch (g) {
             case 1: CKV_ATTN(float, 1);

@@ -15,6 +15,24 @@ constexpr int MAX_ASSIGN_CPAD = 640;  // centroid rows the assignment keeps resi
 constexpr long long WAIT_LIMIT = 2000000000LL;  // SM cycles before a bounded wait gives up
 
 inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while the previous kernel of the stream is still running; it must call
+// ptx::grid_dependency_wait() before touching memory that kernel writes.
+template <typename... P, typename... A>
+cudaError_t launch_dependent(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, A&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<A&&>(args)...);
+}
 inline int ceil_div(int x, int m) { return (x + m - 1) / m; }
 
 }  // namespace ckv
@@ -93,7 +111,7 @@ int attention_rows_per_split(int kv_dtype, int g);
 int attention_mma_rows_per_tile();
 cudaError_t launch_attention_mma(const void* q, const void* K, const void* V, const int32_t* idx,
                                  const int32_t* count, int units, int g, int max_len, int sinks, int clustered_end,
-                                 int cur_len, int B, float* out, float* part, int max_slots, int32_t* dev_err,
-                                 int num_sms, cudaStream_t s);
+                                 int cur_len, int B, float* out, float* part, int32_t* counters, int max_slots,
+                                 int32_t* dev_err, int num_sms, cudaStream_t s);
 
 }  // namespace ckv
