@@ -41,6 +41,9 @@ METRIC = "sparse-decode tokens/s at 32k ctx, B=1024; K-means ms/layer; % of HBM 
 # launch is this ratio times its algorithmic bytes (both grow with the attended
 # rows).  Set to None whenever the kernel changes until it is captured again.
 ATTN_TRAFFIC_PER_ALG_BYTE = 146.745 / 143.53
+# Same for the whole decode step (--path step); None: not captured as one unit.
+STEP_TRAFFIC_PER_ALG_BYTE = None
+STEP_TRAFFIC_SOURCE = "not captured for the whole step"
 ATTN_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch (decode step 41, "
                        "146.7 MB for 143.5 MB algorithmic), scaled to the mean launch by algorithmic bytes")
 WORKLOAD = "decode_32k"
@@ -58,6 +61,9 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget")
     p.add_argument("--units", type=int, default=0, help="override the unit count (small profiling cases)")
     p.add_argument("--decode-steps", type=int, default=0, help="override the decode steps (profiling)")
+    p.add_argument("--path", choices=["separate", "step"], default="separate",
+                   help="decode step as ckv_select + ckv_sparse_decode_attn (per-kernel events), or one "
+                        "ckv_decode_step call")
     return p.parse_args()
 
 
@@ -180,10 +186,12 @@ def run_ours(args, w, rank, world, device):
     torch.cuda.synchronize()
     s = torch.cuda.Stream()
     g_pre, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-    # per-kernel durations: event nodes around the select and attention launches
-    # of every EVERY-th decode step (a uniform sample; events on every step
-    # would themselves slow the loop)
+    # per-kernel durations: event nodes around the ckv_decode_step calls (step
+    # path) or the select and attention launches (separate path) of every
+    # EVERY-th decode step (a uniform sample; events on every step would
+    # themselves slow the loop)
     EVERY = 16
+    one_call = args.path == "step"
     sampled = [t for t in range(T) if t % EVERY == 0]
     ev = {t: [torch.cuda.Event(enable_timing=True) for _ in range(3)] for t in sampled}
     for e3 in ev.values():  # torch creates the CUDA event on first record
@@ -201,12 +209,18 @@ def run_ours(args, w, rank, world, device):
                 q = Q[t]
                 if t in ev:
                     ext.record(ev[t][0], s)
-                ctx.select(q, B, idx, cnt)
-                if t in ev:
-                    ext.record(ev[t][1], s)
-                ctx.sparse_decode_attn(q, K, V, idx, cnt, B, L + t + 1, out)
-                if t in ev:
-                    ext.record(ev[t][2], s)
+                if one_call:
+                    ctx.decode_step(q, K, V, B, L + t + 1, idx, cnt, out)
+                    if t in ev:
+                        ext.record(ev[t][1], s)
+                        ext.record(ev[t][2], s)
+                else:
+                    ctx.select(q, B, idx, cnt)
+                    if t in ev:
+                        ext.record(ev[t][1], s)
+                    ctx.sparse_decode_attn(q, K, V, idx, cnt, B, L + t + 1, out)
+                    if t in ev:
+                        ext.record(ev[t][2], s)
     C_at = [w.C + w.c_plus * (t // w.m) for t in range(T)]
     p0, p1, p2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
 
@@ -253,8 +267,11 @@ def run_ours(args, w, rank, world, device):
     res = dict(step_ms=sum(step_ms) / len(step_ms), prefill_ms=statistics.mean(sample["prefill"]),
                decode_ms=statistics.mean(sample["decode"]), select_ms=statistics.mean(sample["select"]),
                attn_ms=statistics.mean(sample["attn"]), wall_s=wall, clocks=clocks,
+               step_launch_ms=statistics.mean(a + b for a, b in zip(sample["select"], sample["attn"])),
                launches=(launches["prefill"] + launches["decode"]) * args.steps)
     res["attn_bytes_per_launch"] = statistics.mean(decode_bytes(w, t, C_at[t])[0] for t in sampled)
+    res["step_bytes_per_launch"] = statistics.mean(decode_bytes(w, t, C_at[t])[1] for t in sampled)
+    res["one_call"] = one_call
     res["decode_bytes_per_step"] = sum(decode_bytes(w, t, C_at[t])[1] for t in range(T)) / T
     res["assign_ms"] = time_assign(ctx, w, K)
     res["recall"] = selection_recall(ctx, w, K, Q)
@@ -263,7 +280,7 @@ def run_ours(args, w, rank, world, device):
     res["ctx"] = ctx
     res["tensors"] = (K, V, Q)
     if not args.no_e2e:
-        res["e2e"] = run_e2e(ctx, w, K, V, Q)
+        res["e2e"] = run_e2e(ctx, w, K, V, Q, one_call)
     return res
 
 
@@ -345,7 +362,7 @@ def full_kv_attention(w, K, V, Q, reps=5):
             "what": "attention over all L tokens of every unit with the same kernel (idx = every prompt token)"}
 
 
-def run_e2e(ctx, w, K, V, Q):
+def run_e2e(ctx, w, K, V, Q, one_call=False):
     """The same job through the public API from pinned host buffers: upload the
     prompt K/V, prefill clustering, then per decode step upload q and the new
     K/V row of every unit, select, attend, and read the output back."""
@@ -378,8 +395,11 @@ def run_e2e(ctx, w, K, V, Q):
             qd.copy_(Qh[t], non_blocking=True)
             Kd[:, L + t].copy_(knew[t], non_blocking=True)
             Vd[:, L + t].copy_(vnew[t], non_blocking=True)
-            ctx.select(qd, B, idx, cnt)
-            ctx.sparse_decode_attn(qd, Kd, Vd, idx, cnt, B, L + t + 1, out)
+            if one_call:
+                ctx.decode_step(qd, Kd, Vd, B, L + t + 1, idx, cnt, out)
+            else:
+                ctx.select(qd, B, idx, cnt)
+                ctx.sparse_decode_attn(qd, Kd, Vd, idx, cnt, B, L + t + 1, out)
             outh[t].copy_(out, non_blocking=True)
         torch.cuda.synchronize()
 
@@ -462,6 +482,7 @@ def main():
                        f"({w.units} units), d={w.d}, GQA {w.g}, prompt L={w.L}, {w.decode_steps} decode "
                        f"steps, B={w.B}, C={w.C} + {w.c_plus} every {w.m} steps, {w.iters} Lloyd iterations",
            "units": w.units, "L": w.L, "decode_steps": w.decode_steps, "B": w.B, "C": w.C,
+           "path": "ckv_decode_step" if args.path == "step" else "ckv_select + ckv_sparse_decode_attn",
            "l2": "inputs larger than L2: 4.4 GB of K/V and 268 MB of queries resident; every decode "
                  "step gathers ~166 MB of scattered rows (L2 is 129 MB); no flush"}
 
@@ -502,7 +523,32 @@ def main():
         step_ms, prefill_ms, decode_ms = t.tolist()
     T = w.decode_steps
     value = world * T / (step_ms / 1000.0)
-    attn_gbs = r["attn_bytes_per_launch"] / (r["attn_ms"] / 1000.0) / 1e9
+    if r["one_call"]:
+        # one ckv_decode_step call per step: its launch window covers the whole
+        # step; its bytes are those of the whole step
+        step_gbs = r["step_bytes_per_launch"] / (r["step_launch_ms"] / 1000.0) / 1e9
+        roofline = {"bound": "hbm", "kernel": "sel_kernel + attn_mma_kernel + attn_mma_combine_kernel (one "
+                                              "ckv_decode_step: scoring, selection, gather, split-K attention)",
+                    "achieved": step_gbs, "peak": hbm, "unit": "GB/s", "frac": step_gbs / hbm,
+                    "traffic": (STEP_TRAFFIC_PER_ALG_BYTE * r["step_bytes_per_launch"]
+                                if STEP_TRAFFIC_PER_ALG_BYTE else None),
+                    "traffic_source": STEP_TRAFFIC_SOURCE,
+                    "bytes_per_launch": r["step_bytes_per_launch"],
+                    "launch_us": 1000.0 * r["step_launch_ms"], "peak_kind": peak_kind,
+                    "timing": "CUDA events around the decode-step launch of every 16th decode step, inside "
+                              "the timed graph"}
+    else:
+        attn_gbs = r["attn_bytes_per_launch"] / (r["attn_ms"] / 1000.0) / 1e9
+        roofline = {"bound": "hbm", "kernel": "attn_mma_kernel + attn_mma_combine_kernel (gather + split-K "
+                                              "attention)",
+                    "achieved": attn_gbs, "peak": hbm, "unit": "GB/s", "frac": attn_gbs / hbm,
+                    "traffic": (ATTN_TRAFFIC_PER_ALG_BYTE * r["attn_bytes_per_launch"]
+                                if ATTN_TRAFFIC_PER_ALG_BYTE else None),
+                    "traffic_source": ATTN_TRAFFIC_SOURCE,
+                    "bytes_per_launch": r["attn_bytes_per_launch"],
+                    "launch_us": 1000.0 * r["attn_ms"], "peak_kind": peak_kind,
+                    "timing": "CUDA events around the attention launch (+ its combine kernel) of "
+                              "every 16th decode step, inside the timed graph"}
     decode_gbs = r["decode_bytes_per_step"] / (decode_ms / T / 1000.0) / 1e9
     kflops, kbytes = kmeans_flops_bytes(w)
     assign_flops = kflops / w.iters
@@ -519,16 +565,7 @@ def main():
         "kmeans_roofline": {"tflops": kflops / (prefill_ms / 1000.0) / 1e12,
                             "peak_tflops": meas.get("bf16_tflops_sustained", 1700.0),
                             "bytes_gbs": kbytes / (prefill_ms / 1000.0) / 1e9},
-        "roofline": {"bound": "hbm", "kernel": "attn_mma_kernel + attn_mma_combine_kernel (gather + "
-                                               "split-K attention)",
-                     "achieved": attn_gbs, "peak": hbm, "unit": "GB/s", "frac": attn_gbs / hbm,
-                     "traffic": (ATTN_TRAFFIC_PER_ALG_BYTE * r["attn_bytes_per_launch"]
-                                 if ATTN_TRAFFIC_PER_ALG_BYTE else None),
-                     "traffic_source": ATTN_TRAFFIC_SOURCE,
-                     "bytes_per_launch": r["attn_bytes_per_launch"],
-                     "launch_us": 1000.0 * r["attn_ms"], "peak_kind": peak_kind,
-                     "timing": "CUDA events around the attention launch (+ its combine kernel) of "
-                               "every 16th decode step, inside the timed graph"},
+        "roofline": roofline,
         "assign_roofline": {"bound": "tensor", "kernel": "assign_tc_kernel",
                             "achieved": assign_flops / (r["assign_ms"] / 1000.0) / 1e12,
                             "peak": meas.get("bf16_tflops", 1900.0), "unit": "TFLOP/s",
@@ -537,7 +574,8 @@ def main():
         "recall": r["recall"],
         "full_kv": dict(r["full_kv"], decode_speedup=r["full_kv"]["attention_us"] / (1000.0 * decode_ms / T)),
         "phase_ms": {"prefill_clustering": prefill_ms, "decode_loop": decode_ms},
-        "per_launch_us": {"select": 1000.0 * r["select_ms"], "attention": 1000.0 * r["attn_ms"]},
+        "per_launch_us": ({"decode_step": 1000.0 * r["step_launch_ms"]} if r["one_call"] else
+                          {"select": 1000.0 * r["select_ms"], "attention": 1000.0 * r["attn_ms"]}),
         "gpu_launches": r["launches"], "clocks": r["clocks"],
     }
     if "e2e" in r:

@@ -192,6 +192,14 @@ ckv_status ckv_sparse_decode_attn(ckv_ctx* ctx, const void* q, int32_t q_dtype, 
                                   const void* V, const int32_t* idx, const int32_t* count,
                                   int32_t B, int32_t cur_len, float* out, void* stream);
 
+/* One whole decode step of every unit in one call: ckv_select followed by
+ * ckv_sparse_decode_attn on the same stream (the attention kernel is a
+ * dependent launch of the selection kernel).  Arguments, layouts and errors as
+ * for those two calls; idx [units][B], count [units] and out are written. */
+ckv_status ckv_decode_step(ckv_ctx* ctx, const void* q, int32_t q_dtype, const void* K, const void* V,
+                           int32_t B, int32_t cur_len, int32_t* idx, int32_t* count, float* out,
+                           void* stream);
+
 /* Sparse decode attention that allocates nothing and needs no context.
  * The ClusterKV paper has no counterpart of this call; it exists for callers
  * that cannot allocate device memory: code running while a CUDA graph is

@@ -32,6 +32,7 @@ SIGNATURES = {
     "ckv_select_scored": ([_P, _P, _I, _P, _P, _P], _I),
     "ckv_select": ([_P, _P, _I, _I, _P, _P, _P], _I),
     "ckv_sparse_decode_attn": ([_P, _P, _I, _P, _P, _P, _P, _I, _I, _P, _P], _I),
+    "ckv_decode_step": ([_P, _P, _I, _P, _P, _I, _I, _P, _P, _P, _P], _I),
     "ckv_get_info": ([_P, _P], _I),
     "ckv_export_clusters": ([_P, _P, _P, _P, _P, _P, _P], _I),
     "ckv_import_clusters": ([_P, _I, _I, _P, _P, _P, _P, _P], _I),
@@ -171,6 +172,10 @@ class Context:
         _check(lib().ckv_sparse_decode_attn(self.handle, ptr(q), _dtype_code(q), ptr(K), ptr(V),
                                             ptr(idx), ptr(count), B, cur_len, ptr(out),
                                             _stream(stream)), "ckv_sparse_decode_attn")
+
+    def decode_step(self, q, K, V, B: int, cur_len: int, idx, count, out, stream=None):
+        _check(lib().ckv_decode_step(self.handle, ptr(q), _dtype_code(q), ptr(K), ptr(V), B, cur_len, ptr(idx),
+                                     ptr(count), ptr(out), _stream(stream)), "ckv_decode_step")
 
     # -- state -----------------------------------------------------------------
     def info(self) -> Info:

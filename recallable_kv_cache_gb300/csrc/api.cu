@@ -283,6 +283,29 @@ ckv_status ckv_sparse_decode_attn(ckv_ctx* ctx, const void* q, int32_t q_dtype, 
     return cuda_status(e);
 }
 
+ckv_status ckv_decode_step(ckv_ctx* ctx, const void* q, int32_t q_dtype, const void* K, const void* V, int32_t B,
+                           int32_t cur_len, int32_t* idx, int32_t* count, float* out, void* stream) {
+    if (!ctx || !q || !K || !V || !idx || !count || !out) return CKV_ERR_ARG;
+    if (q_dtype != ctx->cfg.kv_dtype) return CKV_ERR_DTYPE;
+    if (!aligned16(q) || !aligned16(K) || !aligned16(V) || !aligned16(out)) return CKV_ERR_ALIGN;
+    if (ctx->n_clusters <= 0 || ctx->clustered_end <= ctx->cfg.sinks) return CKV_ERR_STATE;
+    if (B < 0) return CKV_ERR_ARG;
+    if (B > ctx->cfg.max_budget) return CKV_ERR_CAPACITY;
+    if (cur_len < ctx->clustered_end || cur_len > ctx->cfg.max_len) return CKV_ERR_ARG;
+    if (cur_len - ctx->clustered_end > 2 * ctx->cfg.m) return CKV_ERR_CAPACITY;
+    if (ctx->n_clusters > MAX_SELECT_CLUSTERS) return CKV_ERR_UNIMPLEMENTED;
+    cudaStream_t s = (cudaStream_t)stream;
+    ctx->last_stream = s;
+    // selection, then attention (a dependent launch: it is scheduled while the
+    // selection drains and waits for it on the device)
+    cudaError_t e = launch_select(ctx, q, nullptr, 0, ctx->n_clusters, B, idx, count, s);
+    if (e == cudaSuccess)
+        e = launch_attention(q, K, V, idx, count, ctx->cfg.units, ctx->cfg.g, ctx->cfg.kv_dtype, ctx->cfg.max_len,
+                             ctx->cfg.sinks, ctx->clustered_end, cur_len, B, out, ctx->attn_part, ctx->attn_cnt,
+                             ctx->max_splits, ctx->dev_err, ctx->num_sms, s);
+    return cuda_status(e);
+}
+
 ckv_status ckv_get_info(ckv_ctx* ctx, ckv_info* info) {
     if (!ctx || !info) return CKV_ERR_ARG;
     info->n_clusters = ctx->n_clusters;

@@ -222,3 +222,31 @@ def test_select_large_cluster_counts(C):
     for u in range(U):
         assert torch.equal(i1[u, :c1[u]], i2[u, :c2[u]])
     ctx.close()
+
+
+def test_decode_step_equals_select_then_attention(case):
+    """ckv_decode_step (selection then attention in one call) gives the idx /
+    count of ckv_select and the output of ckv_sparse_decode_attn; three steps
+    in a row."""
+    w, ctx = case["w"], case["ctx"]
+    pend = CASES[case["name"]][5]
+    for qi in range(3):
+        q = case["Q"][qi].cuda().contiguous()
+        cur_len = w.L + (pend if qi != 1 else 0)
+        i1 = torch.full((w.units, w.B), -3, dtype=torch.int32, device="cuda")
+        c1 = torch.empty(w.units, dtype=torch.int32, device="cuda")
+        o1 = torch.empty(w.units, w.g, 128, dtype=torch.float32, device="cuda")
+        ctx.select(q, w.B, i1, c1)
+        ctx.sparse_decode_attn(q, case["Kd"], case["Vd"], i1, c1, w.B, cur_len, o1)
+        i2, c2, o2 = torch.full_like(i1, -3), torch.empty_like(c1), torch.empty_like(o1)
+        ctx.decode_step(q, case["Kd"], case["Vd"], w.B, cur_len, i2, c2, o2)
+        torch.cuda.synchronize()
+        assert ctx.device_error() == 0
+        assert torch.equal(c1, c2) and torch.equal(i1, i2)
+        assert (o1 - o2).abs().max().item() <= 1e-5
+        got = to64(o2)
+        idx, cnt = i2.cpu().numpy(), c2.cpu().numpy()
+        for u in range(w.units):
+            toks = ck.attention_tokens(16, w.L, cur_len, idx[u, :cnt[u]])
+            want = ck.sparse_attention(to64(case["Q"][qi][u]), to64(case["K"][u]), to64(case["V"][u]), toks)
+            assert np.abs(got[u] - want).max() <= ATTN_TOL[w.dtype]

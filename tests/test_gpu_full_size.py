@@ -140,8 +140,14 @@ def test_decode_step_sampled(full):
         assert bool((cnt == min(w.B, w.L - w.sinks)).all())
         out = torch.empty(w.units, w.g, w.d, dtype=torch.float32, device="cuda")
         ctx.sparse_decode_attn(q, K, V, idx, cnt, w.B, cur_len, out)
+        # the whole step in one call: same selection, same output
+        idx3, cnt3 = torch.full_like(idx, -1), torch.empty_like(cnt)
+        out3 = torch.empty_like(out)
+        ctx.decode_step(q, K, V, w.B, cur_len, idx3, cnt3, out3)
         torch.cuda.synchronize()
         assert ctx.device_error() == 0
+        assert torch.equal(cnt, cnt3) and torch.equal(idx, idx3)
+        assert (out - out3).abs().max().item() <= 1e-5
         scores, idx_h, cnt_h, out_h = sc.cpu().numpy(), idx.cpu().numpy(), cnt.cpu().numpy(), to64(out)
         for u in full["samples"]:
             s = unit_state(st, u)
