@@ -350,16 +350,17 @@ __global__ void __launch_bounds__(256) segsum_kernel(const T* __restrict__ K, in
     const int sub = lane / LPR, li = lane % LPR;
     Kahan acc[CPL];
     const T* Ku = K + (size_t)u * max_len * D + li * CPL;
-    for (int r0 = sub; r0 < rows; r0 += 4 * RPI) {
-        uint4 w[4];
+    constexpr int SUNR = 8;  // row loads in flight per lane
+    for (int r0 = sub; r0 < rows; r0 += SUNR * RPI) {
+        uint4 w[SUNR];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < SUNR; ++q) {
             const int r = r0 + q * RPI;
             w[q] = r < rows ? *reinterpret_cast<const uint4*>(Ku + (size_t)toks[warp][r] * D)
                             : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < SUNR; ++q) {
             if (r0 + q * RPI >= rows) break;
             if constexpr (sizeof(T) == 2) {
                 const uint32_t ww[4] = {w[q].x, w[q].y, w[q].z, w[q].w};
