@@ -61,6 +61,8 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget")
     p.add_argument("--units", type=int, default=0, help="override the unit count (small profiling cases)")
     p.add_argument("--decode-steps", type=int, default=0, help="override the decode steps (profiling)")
+    p.add_argument("--sync-incremental", action="store_true",
+                   help="cluster the new tokens inline instead of on a side stream overlapping the next step")
     p.add_argument("--path", choices=["separate", "step"], default="separate",
                    help="decode step as ckv_select + ckv_sparse_decode_attn (per-kernel events), or one "
                         "ckv_decode_step call")
@@ -140,7 +142,7 @@ class ExternalEvents:
 
 
 # ----------------------------------------------------------------------------- algorithmic bytes
-def decode_bytes(w, step: int, C: int):
+def decode_bytes(w, step: int, C: int, async_incr: bool = False):
     """Algorithmic HBM bytes of decode step `step` for all units: (attention, whole step).
     Attention reads every attended K and V row once (bf16, 256 B each) for all
     g heads, the indices, q, and writes out (fp32).  Scoring reads the bf16
@@ -148,6 +150,8 @@ def decode_bytes(w, step: int, C: int):
     offsets and the selected perm entries, writes idx and count."""
     U, g, d, B = w.units, w.g, w.d, w.B
     pend = step % w.m + 1
+    if async_incr and step >= w.m and step % w.m == 0:
+        pend += w.m  # the block being clustered on the side stream is still pending
     rows = w.sinks + pend + B
     attn = U * (rows * 2 * d * 2 + B * 4 + 4 + g * d * 2 + g * d * 4)
     score = U * (C * d * 2 + g * d * 2 + C * 4)
@@ -185,6 +189,8 @@ def run_ours(args, w, rank, world, device):
     ctx.cluster_prefill(K, L, w.C)
     torch.cuda.synchronize()
     s = torch.cuda.Stream()
+    side = torch.cuda.Stream()
+    fork = torch.cuda.Event()
     g_pre, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     # per-kernel durations: event nodes around the ckv_decode_step calls (step
     # path) or the select and attention launches (separate path) of every
@@ -203,9 +209,20 @@ def run_ours(args, w, rank, world, device):
         with torch.cuda.graph(g_pre, stream=s):
             ctx.cluster_prefill(K, L, w.C)
         with torch.cuda.graph(g_dec, stream=s):
+            commit_at = -1
             for t in range(T):
                 if t > 0 and t % w.m == 0:
-                    ctx.cluster_incremental(K, L + t - w.m)
+                    if args.sync_incremental:
+                        ctx.cluster_incremental(K, L + t - w.m)
+                    else:
+                        # fork a side stream: the clustering overlaps this step,
+                        # whose selection still sees the previous clusters
+                        fork.record(s)
+                        side.wait_event(fork)
+                        ctx.cluster_incremental_begin(K, L + t - w.m, stream=side)
+                        commit_at = t + 1
+                if t == commit_at:
+                    ctx.cluster_incremental_commit(stream=s)
                 q = Q[t]
                 if t in ev:
                     ext.record(ev[t][0], s)
@@ -221,7 +238,9 @@ def run_ours(args, w, rank, world, device):
                     ctx.sparse_decode_attn(q, K, V, idx, cnt, B, L + t + 1, out)
                     if t in ev:
                         ext.record(ev[t][2], s)
-    C_at = [w.C + w.c_plus * (t // w.m) for t in range(T)]
+    # clusters visible at step t (an asynchronous clustering begun at step t is
+    # committed before step t + 1)
+    C_at = [w.C + w.c_plus * ((t // w.m) if args.sync_incremental else max(0, (t - 1) // w.m)) for t in range(T)]
     p0, p1, p2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
 
     def one_step(sample):
@@ -269,10 +288,11 @@ def run_ours(args, w, rank, world, device):
                attn_ms=statistics.mean(sample["attn"]), wall_s=wall, clocks=clocks,
                step_launch_ms=statistics.mean(a + b for a, b in zip(sample["select"], sample["attn"])),
                launches=(launches["prefill"] + launches["decode"]) * args.steps)
-    res["attn_bytes_per_launch"] = statistics.mean(decode_bytes(w, t, C_at[t])[0] for t in sampled)
-    res["step_bytes_per_launch"] = statistics.mean(decode_bytes(w, t, C_at[t])[1] for t in sampled)
+    ai = not args.sync_incremental
+    res["attn_bytes_per_launch"] = statistics.mean(decode_bytes(w, t, C_at[t], ai)[0] for t in sampled)
+    res["step_bytes_per_launch"] = statistics.mean(decode_bytes(w, t, C_at[t], ai)[1] for t in sampled)
     res["one_call"] = one_call
-    res["decode_bytes_per_step"] = sum(decode_bytes(w, t, C_at[t])[1] for t in range(T)) / T
+    res["decode_bytes_per_step"] = sum(decode_bytes(w, t, C_at[t], ai)[1] for t in range(T)) / T
     res["assign_ms"] = time_assign(ctx, w, K)
     res["recall"] = selection_recall(ctx, w, K, Q)
     res["full_kv"] = full_kv_attention(w, K, V, Q)
@@ -483,6 +503,8 @@ def main():
                        f"steps, B={w.B}, C={w.C} + {w.c_plus} every {w.m} steps, {w.iters} Lloyd iterations",
            "units": w.units, "L": w.L, "decode_steps": w.decode_steps, "B": w.B, "C": w.C,
            "path": "ckv_decode_step" if args.path == "step" else "ckv_select + ckv_sparse_decode_attn",
+           "incremental": "inline before the step" if args.sync_incremental else
+                          "side stream: begun at the step, overlapping it; committed before the next step",
            "l2": "inputs larger than L2: 4.4 GB of K/V and 268 MB of queries resident; every decode "
                  "step gathers ~166 MB of scattered rows (L2 is 129 MB); no flush"}
 

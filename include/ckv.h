@@ -142,6 +142,22 @@ ckv_status ckv_cluster_prefill(ckv_ctx* ctx, const void* K, int32_t L, int32_t n
 ckv_status ckv_cluster_incremental(ckv_ctx* ctx, const void* K, int32_t start, int32_t m,
                                    int32_t c_plus, void* stream);
 
+/* The same incremental clustering split in two, so that it can overlap decode
+ * work (ClusterKV page, section "Semantic clustering optimisation", Fig. 6:
+ * clustering runs asynchronously, overlapped with the model's other work).
+ * _begin launches the clustering on `stream` (typically a side stream forked
+ * from the decode stream) and writes the new centroids and perm segment where
+ * no decode call reads them; until _commit, ckv_select, ckv_sparse_decode_attn
+ * and ckv_decode_step keep using the previous clusters and treat the m tokens
+ * as pending (attended in full).  _commit makes `stream` wait for the
+ * clustering and then publishes it (n_clusters += c_plus, clustered_end +=
+ * m).  Errors as for ckv_cluster_incremental; CKV_ERR_STATE for a second
+ * _begin before _commit, a _commit with nothing begun, or
+ * ckv_cluster_incremental while one is pending. */
+ckv_status ckv_cluster_incremental_begin(ckv_ctx* ctx, const void* K, int32_t start, int32_t m,
+                                         int32_t c_plus, void* stream);
+ckv_status ckv_cluster_incremental_commit(ckv_ctx* ctx, void* stream);
+
 /* One assignment step with the context's current n_clusters centroids:
  * labels[u][i] = argmax_c cos(k_{sinks+i}, mu_c) for i < L - sinks, ties to
  * the lower index (section "Clustering in semantic space", clustering

@@ -33,6 +33,8 @@ SIGNATURES = {
     "ckv_select": ([_P, _P, _I, _I, _P, _P, _P], _I),
     "ckv_sparse_decode_attn": ([_P, _P, _I, _P, _P, _P, _P, _I, _I, _P, _P], _I),
     "ckv_decode_step": ([_P, _P, _I, _P, _P, _I, _I, _P, _P, _P, _P], _I),
+    "ckv_cluster_incremental_begin": ([_P, _P, _I, _I, _I, _P], _I),
+    "ckv_cluster_incremental_commit": ([_P, _P], _I),
     "ckv_get_info": ([_P, _P], _I),
     "ckv_export_clusters": ([_P, _P, _P, _P, _P, _P, _P], _I),
     "ckv_import_clusters": ([_P, _I, _I, _P, _P, _P, _P, _P], _I),
@@ -146,6 +148,17 @@ class Context:
         c_plus = self.cfg.c_plus if c_plus is None else c_plus
         _check(lib().ckv_cluster_incremental(self.handle, ptr(K), start, m, c_plus, _stream(stream)),
                "ckv_cluster_incremental")
+
+    def cluster_incremental_begin(self, K, start: int, m: int | None = None, c_plus: int | None = None,
+                                  stream=None):
+        m = self.cfg.m if m is None else m
+        c_plus = self.cfg.c_plus if c_plus is None else c_plus
+        _check(lib().ckv_cluster_incremental_begin(self.handle, ptr(K), start, m, c_plus, _stream(stream)),
+               "ckv_cluster_incremental_begin")
+
+    def cluster_incremental_commit(self, stream=None):
+        _check(lib().ckv_cluster_incremental_commit(self.handle, _stream(stream)),
+               "ckv_cluster_incremental_commit")
 
     def kmeans_assign(self, K, L: int, labels, stream=None):
         _check(lib().ckv_kmeans_assign(self.handle, ptr(K), L, ptr(labels), _stream(stream)),

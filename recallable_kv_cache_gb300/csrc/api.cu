@@ -37,6 +37,7 @@ void free_all(ckv_ctx* c) {
                     c->seg_part, c->scores, c->attn_part, c->attn_cnt, c->dev_err, c->assign_best};
     for (void* p : ptrs)
         if (p) cudaFree(p);
+    if (c->pend_done) cudaEventDestroy(c->pend_done);
 }
 
 ckv_status check_kv(const ckv_ctx* ctx, const void* K) {
@@ -104,6 +105,9 @@ ckv_status ckv_create(const ckv_config* cfg, ckv_ctx** out) {
     c->max_splits = ceil_div(c->attn_rows, attention_rows_per_split(cfg->kv_dtype, cfg->g));
     c->elem = cfg->kv_dtype == CKV_BF16 ? 2 : 4;
     c->last_stream = nullptr;
+    c->pend_m = 0;
+    c->pend_c_plus = 0;
+    c->pend_done = nullptr;
 
     const size_t cd = (size_t)c->cmax * D;
     bool ok = alloc(&c->mu32, U * cd) == cudaSuccess;
@@ -126,6 +130,7 @@ ckv_status ckv_create(const ckv_config* cfg, ckv_ctx** out) {
     ok = ok && alloc(&c->attn_part, U * c->max_splits * cfg->g * (D + 2)) == cudaSuccess;
     ok = ok && alloc(&c->attn_cnt, U) == cudaSuccess;
     ok = ok && alloc(&c->dev_err, 1) == cudaSuccess;
+    ok = ok && cudaEventCreateWithFlags(&c->pend_done, cudaEventDisableTiming) == cudaSuccess;
     if (cfg->kv_dtype == CKV_BF16 && c->cmax_pad > MAX_ASSIGN_CPAD)
         ok = ok && alloc(&c->assign_best, U * c->ntok) == cudaSuccess;
     if (ok) {
@@ -185,6 +190,7 @@ ckv_status ckv_cluster_incremental(ckv_ctx* ctx, const void* K, int32_t start, i
                                    void* stream) {
     ckv_status st = check_kv(ctx, K);
     if (st != CKV_OK) return st;
+    if (ctx->pend_m > 0) return CKV_ERR_STATE;
     if (ctx->n_clusters <= 0 || start != ctx->clustered_end) return CKV_ERR_STATE;
     if (c_plus < 1 || c_plus > 16 || m < c_plus || m > MAX_INCR_M || start + m > ctx->cfg.max_len)
         return CKV_ERR_ARG;
@@ -196,6 +202,41 @@ ckv_status ckv_cluster_incremental(ckv_ctx* ctx, const void* K, int32_t start, i
     if (e != cudaSuccess) return CKV_ERR_CUDA;
     ctx->n_clusters += c_plus;
     ctx->clustered_end += m;
+    return CKV_OK;
+}
+
+ckv_status ckv_cluster_incremental_begin(ckv_ctx* ctx, const void* K, int32_t start, int32_t m, int32_t c_plus,
+                                         void* stream) {
+    ckv_status st = check_kv(ctx, K);
+    if (st != CKV_OK) return st;
+    if (ctx->pend_m > 0) return CKV_ERR_STATE;
+    if (ctx->n_clusters <= 0 || start != ctx->clustered_end) return CKV_ERR_STATE;
+    if (c_plus < 1 || c_plus > 16 || m < c_plus || m > MAX_INCR_M || start + m > ctx->cfg.max_len)
+        return CKV_ERR_ARG;
+    if (ctx->n_clusters + c_plus > ctx->cmax) return CKV_ERR_CAPACITY;
+    cudaStream_t s = (cudaStream_t)stream;
+    // the new clusters go to slots [n_clusters, n_clusters + c_plus) and the
+    // perm segment after the clustered tokens: nothing the decode calls read
+    // until the commit advances the counters
+    const int csr_base = ctx->clustered_end - ctx->cfg.sinks;
+    cudaError_t e = launch_incremental(ctx, K, start, m, c_plus, ctx->n_clusters, csr_base, s);
+    if (e == cudaSuccess) e = cudaEventRecord(ctx->pend_done, s);
+    if (e != cudaSuccess) return CKV_ERR_CUDA;
+    ctx->pend_m = m;
+    ctx->pend_c_plus = c_plus;
+    return CKV_OK;
+}
+
+ckv_status ckv_cluster_incremental_commit(ckv_ctx* ctx, void* stream) {
+    if (!ctx) return CKV_ERR_ARG;
+    if (ctx->pend_m <= 0) return CKV_ERR_STATE;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaStreamWaitEvent(s, ctx->pend_done, 0) != cudaSuccess) return CKV_ERR_CUDA;
+    ctx->last_stream = s;
+    ctx->n_clusters += ctx->pend_c_plus;
+    ctx->clustered_end += ctx->pend_m;
+    ctx->pend_m = 0;
+    ctx->pend_c_plus = 0;
     return CKV_OK;
 }
 

@@ -55,6 +55,9 @@ struct ckv_ctx {
     int prefill_len;
     int clustered_end;
     cudaStream_t last_stream;
+    // an incremental clustering launched but not yet visible (begin / commit)
+    int pend_c_plus, pend_m;
+    cudaEvent_t pend_done;
 
     // state
     float* mu32;        // [U][cmax][D] centroids (fp32 master)

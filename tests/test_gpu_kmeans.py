@@ -251,3 +251,59 @@ def test_incremental(iters):
                 assert np.array_equal(st["offsets"][u][cs] - seg_lo, inc["offsets"][:4])
                 assert np.array_equal(got_perm, inc["perm"])
                 check_centroids(st["mu"][u][cs], inc["mu"])
+
+
+def test_incremental_begin_commit():
+    """The split incremental clustering: while it is pending the decode calls
+    see the previous clusters (its tokens are attended as pending tokens);
+    after the commit the state is bit-identical to ckv_cluster_incremental's."""
+    from parity import ATTN_TOL
+    from recallable_kv_cache_gb300.ckv import CKVError
+    w = workload("layer_32k", units=2, L=16 + 800, decode_steps=700, C=10, n_centres=10, B=128)
+    K, V = synth.make_kv(w)
+    Q = synth.make_queries(w, 1)
+    Kd, Vd = K.cuda().contiguous(), V.cuda().contiguous()
+    a = make_ctx(2, 4, w.max_len, 18, 128, "bf16")
+    b = make_ctx(2, 4, w.max_len, 18, 128, "bf16")
+    a.cluster_prefill(Kd, w.L, 10)
+    b.cluster_prefill(Kd, w.L, 10)
+    before = export_state(b, 2)
+    a.cluster_incremental(Kd, w.L, 320, 4)
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    ev = torch.cuda.Event()
+    ev.record(main)
+    side.wait_event(ev)
+    b.cluster_incremental_begin(Kd, w.L, 320, 4, stream=side)
+    with pytest.raises(CKVError):
+        b.cluster_incremental_begin(Kd, w.L, 320, 4, stream=side)
+    with pytest.raises(CKVError):
+        b.cluster_incremental(Kd, w.L, 320, 4)
+    inf = b.info()
+    assert inf.n_clusters == 10 and inf.clustered_end == w.L
+    # decode while pending: previous clusters, 330 pending tokens
+    q = Q[0].cuda().contiguous()
+    idx = torch.empty(2, 128, dtype=torch.int32, device="cuda")
+    cnt = torch.empty(2, dtype=torch.int32, device="cuda")
+    out = torch.empty(2, 4, 128, dtype=torch.float32, device="cuda")
+    cur_len = w.L + 330
+    b.decode_step(q, Kd, Vd, 128, cur_len, idx, cnt, out)
+    torch.cuda.synchronize()
+    got, ih, ch = to64(out), idx.cpu().numpy(), cnt.cpu().numpy()
+    for u in range(2):
+        sel, c = ck.select(ck.score(to64(Q[0][u]), before["mu"][u]), before["sizes"][u], before["offsets"][u],
+                           before["perm"][u], 128)
+        assert ch[u] == c
+        toks = ck.attention_tokens(16, w.L, cur_len, ih[u, :c])
+        want = ck.sparse_attention(to64(Q[0][u]), to64(K[u]), to64(V[u]), toks)
+        assert np.abs(got[u] - want).max() <= ATTN_TOL["bf16"]
+    b.cluster_incremental_commit(stream=main)
+    with pytest.raises(CKVError):
+        b.cluster_incremental_commit(stream=main)
+    inf = b.info()
+    assert inf.n_clusters == 14 and inf.clustered_end == w.L + 320
+    sa, sb = export_state(a, 2), export_state(b, 2)
+    for k in ("mu", "mu_hat", "sizes", "offsets", "perm"):
+        assert np.array_equal(sa[k], sb[k]), k
+    a.close()
+    b.close()
