@@ -294,7 +294,8 @@ def run_ours(args, w, rank, world, device):
     res["one_call"] = one_call
     res["decode_bytes_per_step"] = sum(decode_bytes(w, t, C_at[t], ai)[1] for t in range(T)) / T
     res["assign_ms"] = time_assign(ctx, w, K)
-    res["recall"] = selection_recall(ctx, w, K, Q)
+    res["recall"] = selection_recall(lambda q, i, c: ctx.select(q, w.B, i, c), w, K, Q)
+    res["quest"] = quest_comparator(w, K, V, Q)
     res["full_kv"] = full_kv_attention(w, K, V, Q)
     res["w"] = w
     res["ctx"] = ctx
@@ -322,18 +323,18 @@ def time_assign(ctx, w, K, reps=5):
     return a0.elapsed_time(a1) / reps
 
 
-def selection_recall(ctx, w, K, Q, units=(0, 97, 201), queries=(0, 1, 2)):
-    """Recall of the cluster selection against the exact top-B tokens by
-    sum_h q_h . k (a measurement, not part of the path): token recall
-    |S n TopB| / B and attention-mass recall sum_S a / sum_TopB a, a = the full
-    softmax over the clustered prompt tokens averaged over the g heads.  The
-    selection is the library's (prefill clusters, decode step 0 state)."""
+def selection_recall(select, w, K, Q, units=(0, 97, 201), queries=(0, 1, 2), what="prefill clusters"):
+    """Recall of a selection against the exact top-B tokens by sum_h q_h . k
+    (a measurement, not part of the path): token recall |S n TopB| / B and
+    attention-mass recall sum_S a / sum_TopB a, a = the full softmax over the
+    clustered prompt tokens averaged over the g heads.  `select(q, idx, cnt)`
+    runs the library's selection for every unit."""
     idx = torch.empty(w.units, w.B, dtype=torch.int32, device="cuda")
     cnt = torch.empty(w.units, dtype=torch.int32, device="cuda")
     tok, mass = [], []
     for qi in queries:
         q = Q[qi]
-        ctx.select(q, w.B, idx, cnt)
+        select(q, idx, cnt)
         torch.cuda.synchronize()
         for u in units:
             keys = K[u, w.sinks:w.L].float()
@@ -346,7 +347,68 @@ def selection_recall(ctx, w, K, Q, units=(0, 97, 201), queries=(0, 1, 2)):
             tok.append(inter / w.B)
             mass.append((a[sel].sum() / a[top].sum()).item())
     return {"token": statistics.mean(tok), "attention_mass": statistics.mean(mass),
-            "sample": f"{len(units)} units x {len(queries)} queries, prefill clusters, B={w.B}"}
+            "sample": f"{len(units)} units x {len(queries)} queries, {what}, B={w.B}"}
+
+
+def quest_comparator(w, K, V, Q, steps=64):
+    """The page-granular comparator (Quest) on the same units, budget and
+    queries: page bounds of the prompt (pages of 16 tokens), then per step the
+    page weights, the selection of whole pages and the same attention kernel,
+    captured in a graph of `steps` steps (one pending token) and timed; and
+    its recall, measured like the cluster selection's."""
+    from recallable_kv_cache_gb300 import ckv
+    U, L, B, sinks = w.units, w.L, w.B, w.sinks
+    n = L - sinks
+    P = (n + 15) // 16
+    pmax = torch.empty(U, P, w.d, dtype=K.dtype, device="cuda")
+    pmin = torch.empty_like(pmax)
+    scores = torch.empty(U, P, dtype=torch.float32, device="cuda")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ckv.quest_pages(K, L, pmax, pmin)
+    e0.record()
+    ckv.quest_pages(K, L, pmax, pmin)
+    e1.record()
+    torch.cuda.synchronize()
+    build_ms = e0.elapsed_time(e1)
+    pctx = ckv.Context(units=U, g=w.g, max_len=w.max_len, max_clusters=P, max_budget=B, iters=1, m=w.m,
+                       c_plus=w.c_plus)
+    sizes = torch.full((U, P), 16, dtype=torch.int32, device="cuda")
+    sizes[:, -1] = n - 16 * (P - 1)
+    offs = torch.zeros(U, P + 1, dtype=torch.int32, device="cuda")
+    offs[:, 1:] = torch.cumsum(sizes, dim=1)
+    perm = torch.arange(sinks, L, dtype=torch.int32, device="cuda").expand(U, n).contiguous()
+    pctx.import_clusters(P, L, torch.zeros(U, P, w.d, device="cuda"), sizes, offs, perm)
+
+    def select(q, idx, cnt):
+        ckv.quest_score(q, pmax, pmin, scores)
+        pctx.select_scored(scores, B, idx, cnt)
+
+    recall = selection_recall(select, w, K, Q, what="pages of 16 tokens")
+    idx = torch.empty(U, B, dtype=torch.int32, device="cuda")
+    cnt = torch.empty(U, dtype=torch.int32, device="cuda")
+    out = torch.empty(U, w.g, w.d, dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        for t in range(2):
+            select(Q[t], idx, cnt)
+            pctx.sparse_decode_attn(Q[t], K, V, idx, cnt, B, L + 1, out)
+        with torch.cuda.graph(g, stream=s):
+            for t in range(steps):
+                select(Q[t], idx, cnt)
+                pctx.sparse_decode_attn(Q[t], K, V, idx, cnt, B, L + 1, out)
+        g.replay()
+        e0.record(s)
+        for _ in range(3):
+            g.replay()
+        e1.record(s)
+    torch.cuda.synchronize()
+    step_us = 1000.0 * e0.elapsed_time(e1) / (3 * steps)
+    pctx.close()
+    return {"step_us": step_us, "page_bounds_ms": build_ms, "recall": recall,
+            "metadata_bytes_per_step": U * P * 2 * w.d * K.element_size(),
+            "what": "Quest-style pages of 16 tokens: per-channel max / min keys, weight = upper bound of q.k "
+                    "summed over the heads; whole pages up to B; same attention kernel; one pending token"}
 
 
 def full_kv_attention(w, K, V, Q, reps=5):
@@ -595,6 +657,7 @@ def main():
                             "launch_us": 1000.0 * r["assign_ms"], "peak_kind": peak_kind + " (burst: timed alone)"},
         "recall": r["recall"],
         "full_kv": dict(r["full_kv"], decode_speedup=r["full_kv"]["attention_us"] / (1000.0 * decode_ms / T)),
+        "quest": r["quest"],
         "phase_ms": {"prefill_clustering": prefill_ms, "decode_loop": decode_ms},
         "per_launch_us": ({"decode_step": 1000.0 * r["step_launch_ms"]} if r["one_call"] else
                           {"select": 1000.0 * r["select_ms"], "attention": 1000.0 * r["attn_ms"]}),

@@ -216,6 +216,28 @@ ckv_status ckv_decode_step(ckv_ctx* ctx, const void* q, int32_t q_dtype, const v
                            int32_t B, int32_t cur_len, int32_t* idx, int32_t* count, float* out,
                            void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Page-granular comparator (Quest), the baseline the ClusterKV page compares
+ * its recall against (section "Background and design principles", drawbacks
+ * of existing recallable compression; pages of 16 tokens, Fig. 3b).
+ *
+ * The clustered tokens [sinks, L) form n_pages = ceil((L - sinks) / 16) pages
+ * of consecutive tokens (the last may be short).  ckv_quest_pages writes each
+ * page's per-channel maximum and minimum key, page_max / page_min
+ * [units][n_pages][d] of kv_dtype (caller-owned, 16-byte aligned).
+ * ckv_quest_score writes each page's weight, the upper bound of q . k over the
+ * page summed over the g query heads, scores [units][n_pages] float:
+ *   w_p = sum_h sum_i max(q_hi * max_pi, q_hi * min_pi).
+ * The selection is ckv_select_scored on a context whose clusters are the
+ * pages (sizes 16, offsets 16 p, the identity permutation, imported with
+ * ckv_import_clusters), and the attention ckv_sparse_decode_attn.
+ * Errors: CKV_ERR_ARG (L <= sinks, L > max_len, g not 1/2/4/8),
+ * CKV_ERR_DTYPE, CKV_ERR_ALIGN. */
+ckv_status ckv_quest_pages(const void* K, int32_t kv_dtype, int32_t units, int32_t max_len, int32_t sinks,
+                           int32_t L, void* page_max, void* page_min, void* stream);
+ckv_status ckv_quest_score(const void* q, int32_t q_dtype, const void* page_max, const void* page_min,
+                           int32_t units, int32_t g, int32_t n_pages, float* scores, void* stream);
+
 /* Sparse decode attention that allocates nothing and needs no context.
  * The ClusterKV paper has no counterpart of this call; it exists for callers
  * that cannot allocate device memory: code running while a CUDA graph is

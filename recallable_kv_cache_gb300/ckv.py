@@ -33,6 +33,8 @@ SIGNATURES = {
     "ckv_select": ([_P, _P, _I, _I, _P, _P, _P], _I),
     "ckv_sparse_decode_attn": ([_P, _P, _I, _P, _P, _P, _P, _I, _I, _P, _P], _I),
     "ckv_decode_step": ([_P, _P, _I, _P, _P, _I, _I, _P, _P, _P, _P], _I),
+    "ckv_quest_pages": ([_P, _I, _I, _I, _I, _I, _P, _P, _P], _I),
+    "ckv_quest_score": ([_P, _I, _P, _P, _I, _I, _I, _P, _P], _I),
     "ckv_cluster_incremental_begin": ([_P, _P, _I, _I, _I, _P], _I),
     "ckv_cluster_incremental_commit": ([_P, _P], _I),
     "ckv_get_info": ([_P, _P], _I),
@@ -223,3 +225,17 @@ def sparse_decode_attn_noalloc(q, K, V, idx, count, units: int, g: int, max_len:
                                                 ptr(count), units, g, max_len, sinks, clustered_end,
                                                 cur_len, B, ptr(out), ptr(dev_err), _stream(stream)),
            "ckv_sparse_decode_attn_noalloc")
+
+
+def quest_pages(K, L: int, page_max, page_min, sinks: int = 16, stream=None):
+    """Page metadata of the page-granular comparator (see ckv_quest_pages)."""
+    units, max_len = K.shape[0], K.shape[1]
+    _check(lib().ckv_quest_pages(ptr(K), _dtype_code(K), units, max_len, sinks, L, ptr(page_max), ptr(page_min),
+                                 _stream(stream)), "ckv_quest_pages")
+
+
+def quest_score(q, page_max, page_min, scores, stream=None):
+    """Page weights of the page-granular comparator (see ckv_quest_score)."""
+    units, g = q.shape[0], q.shape[1]
+    _check(lib().ckv_quest_score(ptr(q), _dtype_code(q), ptr(page_max), ptr(page_min), units, g,
+                                 page_max.shape[1], ptr(scores), _stream(stream)), "ckv_quest_score")

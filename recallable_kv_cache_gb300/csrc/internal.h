@@ -13,6 +13,7 @@ constexpr int SEG_ROWS = 64;       // rows per centroid-update task
 constexpr int ASSIGN_TILE = 128;   // tokens per tcgen05 assignment tile (MMA M)
 constexpr int MAX_ASSIGN_CPAD = 640;  // centroid rows the assignment keeps resident in smem
 constexpr long long WAIT_LIMIT = 2000000000LL;  // SM cycles before a bounded wait gives up
+constexpr int QUEST_PAGE = 16;     // tokens per page of the page-granular comparator
 
 inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
