@@ -169,11 +169,33 @@ def kmeans_flops_bytes(w):
 
 
 # ----------------------------------------------------------------------------- our path
+def rank_workload(w, rank: int, world: int):
+    """Weak scaling: every rank runs the whole workload on its own units (its
+    own sequences: a seed of its own); units never cross ranks, so the path
+    needs no collective."""
+    return synth.scaled(w, seed=w.seed + 1000 * rank) if world > 1 else w
+
+
+def max_over_ranks(values, world: int, device="cuda"):
+    """Element-wise maximum of a list of floats over all ranks (the job ends
+    when the slowest rank ends)."""
+    if world <= 1:
+        return list(values)
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_value(world: int, decode_steps: int, step_ms: float) -> float:
+    """Whole-job throughput: decode tokens of all ranks / job time (the max
+    over ranks)."""
+    return world * decode_steps / (step_ms / 1000.0)
+
+
 def run_ours(args, w, rank, world, device):
     from recallable_kv_cache_gb300 import ckv
     torch.cuda.set_device(device)
-    if world > 1:  # weak scaling: every rank its own sequence batch
-        w = synth.scaled(w, seed=w.seed + 1000 * rank)
+    w = rank_workload(w, rank, world)
     U, L, B, T = w.units, w.L, w.B, w.decode_steps
     K, V = synth.make_kv(w, device="cuda")
     Q = synth.make_queries(w, T, device="cuda")
@@ -601,12 +623,9 @@ def main():
     w = r["w"]
     hbm, peak_kind, meas = peaks()
     step_ms, prefill_ms, decode_ms = r["step_ms"], r["prefill_ms"], r["decode_ms"]
-    if world > 1:
-        t = torch.tensor([step_ms, prefill_ms, decode_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms, prefill_ms, decode_ms = t.tolist()
+    step_ms, prefill_ms, decode_ms = max_over_ranks([step_ms, prefill_ms, decode_ms], world)
     T = w.decode_steps
-    value = world * T / (step_ms / 1000.0)
+    value = job_value(world, T, step_ms)
     if r["one_call"]:
         # one ckv_decode_step call per step: its launch window covers the whole
         # step; its bytes are those of the whole step
