@@ -226,7 +226,8 @@ def run_ours(args, w, rank, world, device):
         for e in e3:
             e.record(s)
     s.synchronize()
-    launches = {"prefill": 1 + w.iters * 6, "decode": 3 * T + w.n_incremental}
+    # decode: score, select, attention, combine per step + one incremental kernel per block
+    launches = {"prefill": 1 + w.iters * 6, "decode": 4 * T + w.n_incremental}
     with torch.cuda.stream(s):
         with torch.cuda.graph(g_pre, stream=s):
             ctx.cluster_prefill(K, L, w.C)
@@ -630,8 +631,9 @@ def main():
         # one ckv_decode_step call per step: its launch window covers the whole
         # step; its bytes are those of the whole step
         step_gbs = r["step_bytes_per_launch"] / (r["step_launch_ms"] / 1000.0) / 1e9
-        roofline = {"bound": "hbm", "kernel": "sel_kernel + attn_mma_kernel + attn_mma_combine_kernel (one "
-                                              "ckv_decode_step: scoring, selection, gather, split-K attention)",
+        roofline = {"bound": "hbm", "kernel": "score_kernel + sel_kernel + attn_mma_kernel + attn_mma_combine_kernel "
+                                              "(one ckv_decode_step: scoring, selection, gather, split-K "
+                                              "attention)",
                     "achieved": step_gbs, "peak": hbm, "unit": "GB/s", "frac": step_gbs / hbm,
                     "traffic": (STEP_TRAFFIC_PER_ALG_BYTE * r["step_bytes_per_launch"]
                                 if STEP_TRAFFIC_PER_ALG_BYTE else None),

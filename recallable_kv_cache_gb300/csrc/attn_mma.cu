@@ -39,13 +39,6 @@ constexpr unsigned FULL = 0xffffffffu;
 constexpr int MW = 8;   // warps per CTA
 constexpr int TR = 16;  // rows per tile
 
-__device__ __forceinline__ uint4 ldg_stream(const void* p) {
-    uint4 r;
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-        : "l"(p));
-    return r;
-}
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
@@ -373,8 +366,7 @@ __global__ void __launch_bounds__(G * D) attn_mma_combine_kernel(const float* __
 template <int G>
 cudaError_t launch_mma_t(const void* q, const void* K, const void* V, const int32_t* idx, const int32_t* count,
                          int units, int max_len, int sinks, int clustered_end, int cur_len, int B, float* out,
-                         float* part, int32_t* counters, int max_slots, int32_t* dev_err, int num_sms,
-                         cudaStream_t st) {
+                         float* part, int max_slots, int32_t* dev_err, int num_sms, cudaStream_t st) {
     MmaArgs a;
     a.q = static_cast<const __nv_bfloat16*>(q);
     a.K = static_cast<const __nv_bfloat16*>(K);
@@ -390,7 +382,7 @@ cudaError_t launch_mma_t(const void* q, const void* K, const void* V, const int3
     if (a.tpu < 1) a.tpu = 1;
     if (a.tpu > max_slots) return cudaErrorInvalidValue;
     a.total = a.tpu * units;
-    const int sms = num_sms > 0 ? num_sms : 148;
+    const int sms = num_sms > 0 ? num_sms : 152;
     const int warps = sms * MW;
     a.tpw = (a.total + warps - 1) / warps;
     if (a.tpw * (CMB_MAX_SLOTS - 1) < a.tpu) a.tpw = (a.tpu + CMB_MAX_SLOTS - 2) / (CMB_MAX_SLOTS - 1);
@@ -414,11 +406,11 @@ int attention_mma_rows_per_tile() { return TR; }
 
 cudaError_t launch_attention_mma(const void* q, const void* K, const void* V, const int32_t* idx,
                                  const int32_t* count, int units, int g, int max_len, int sinks, int clustered_end,
-                                 int cur_len, int B, float* out, float* part, int32_t* counters, int max_slots,
-                                 int32_t* dev_err, int num_sms, cudaStream_t s) {
+                                 int cur_len, int B, float* out, float* part, int max_slots, int32_t* dev_err,
+                                 int num_sms, cudaStream_t s) {
 #define CKV_MMA(G)                                                                                            \
     return launch_mma_t<G>(q, K, V, idx, count, units, max_len, sinks, clustered_end, cur_len, B, out, part, \
-                           counters, max_slots, dev_err, num_sms, s)
+                           max_slots, dev_err, num_sms, s)
     switch (g) {
         case 1: CKV_MMA(1);
         case 2: CKV_MMA(2);

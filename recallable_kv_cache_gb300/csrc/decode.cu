@@ -1,7 +1,7 @@
 // Decode-step kernels of the ClusterKV path:
 //   score_kernel   cluster scores q . mu (section "Selection at semantic-cluster
 //                  granularity"), HBM-bound stream over the centroid table;
-//   select_kernel  rank clusters, prefix-sum their sizes, trim the last one and
+//   sel_kernel     rank clusters, prefix-sum their sizes, trim the last one and
 //                  compact the token ids (section "Selection and indexing
 //                  mechanism", Fig. 8), one CTA per unit;
 //   attn_kernel    gather of the selected K/V rows with bulk-async copies into
@@ -65,6 +65,8 @@ __global__ void __launch_bounds__(256) score_kernel(const T* __restrict__ q,
     const int u = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int sub = lane / LPR, li = lane % LPR;
+    ptx::grid_dependency_wait();  // q may come from the previous kernel
+    ptx::allow_dependent_launch();
 
     float qs[CPL];
 #pragma unroll
@@ -134,22 +136,20 @@ __device__ __forceinline__ uint64_t rank_key(float s, int c) {
     return ((uint64_t)(~ord) << 32) | (uint32_t)c;                      // descending score, asc c
 }
 
-// One CTA per unit.  Scores (computed here from q and the bf16 centroid copy,
-// or read from the caller) become 64-bit keys (descending score, ascending
-// cluster index) that are sorted by a bitonic network held in registers:
-// exchange distances below 32 use warp shuffles, larger ones shared memory,
-// and distances of at least the block size stay inside a thread (E keys per
-// thread).  The sizes taken in rank order are prefix-summed, the budget cut
-// found, and every output slot p < min(B, total) looks up its rank by binary
-// search and copies its token id from the label-sorted permutation.
-// All global reads except the permutation (q, centroid rows, sizes, offsets)
-// are issued before any of them is used, so they share one round trip.
-template <typename T, int G, int E, bool FROM_SCORES>
+// One CTA per unit.  Scores (from score_kernel or the caller) become 64-bit
+// keys (descending score, ascending cluster index) that are sorted by a
+// bitonic network held in registers: exchange distances below 32 use warp
+// shuffles, larger ones shared memory, and distances of at least the block
+// size stay inside a thread (E keys per thread).  The sizes taken in rank
+// order are prefix-summed, the budget cut found, and every output slot
+// p < min(B, total) looks up its rank by binary search and copies its token id
+// from the label-sorted permutation.  The sizes, offsets and scores are all
+// loaded before any of them is used, so they share one round trip.
+template <int E>
 __global__ void __launch_bounds__(1024, 1) sel_kernel(
-    const T* __restrict__ q, const T* __restrict__ mu, int cmax, const float* __restrict__ scores_in,
-    int sstride, int C, int N, const int32_t* __restrict__ sizes, const int32_t* __restrict__ offsets,
-    const int32_t* __restrict__ perm, int ntok, int B, int32_t* __restrict__ idx,
-    int32_t* __restrict__ count, int32_t* __restrict__ dev_err) {
+    const float* __restrict__ scores_in, int sstride, int cmax, int C, int N, const int32_t* __restrict__ sizes,
+    const int32_t* __restrict__ offsets, const int32_t* __restrict__ perm, int ntok, int B,
+    int32_t* __restrict__ idx, int32_t* __restrict__ count, int32_t* __restrict__ dev_err) {
     extern __shared__ __align__(16) unsigned char sel_smem[];
     uint64_t* sk = reinterpret_cast<uint64_t*>(sel_smem);  // [N]
     int32_t* start = reinterpret_cast<int32_t*>(sk + N);   // [N]
@@ -160,66 +160,24 @@ __global__ void __launch_bounds__(1024, 1) sel_kernel(
     __shared__ int32_t s_tot;
     const int u = blockIdx.x, tid = threadIdx.x, NT = blockDim.x;
     const int lane = tid & 31, warp = tid >> 5, nwarps = NT >> 5;
-    ptx::grid_dependency_wait();    // q, the cluster state and idx may come from the previous kernel
+    ptx::grid_dependency_wait();    // the scores, the cluster state and idx may come from the previous kernel
     ptx::allow_dependent_launch();
 
-    // ---- 1. sizes / offsets (registers first, shared memory after the scores)
+    // ---- 1. sizes / offsets / scores (registers first, shared memory after)
     int szr[E], ofr[E];
+    float scr[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) {
         const int c = e * NT + tid;
         szr[e] = c < C ? sizes[(size_t)u * cmax + c] : 0;
         ofr[e] = c < C ? offsets[(size_t)u * (cmax + 1) + c] : 0;
+        scr[e] = c < C ? scores_in[(size_t)u * sstride + c] : 0.f;
     }
-    // ---- 2. unsorted keys
-    if constexpr (FROM_SCORES) {
-        for (int c = tid; c < N; c += NT) sk[c] = c < C ? rank_key(scores_in[(size_t)u * sstride + c], c) : ~0ull;
-    } else {
-        constexpr int CPL = Vec<T>::N, LPR = D / CPL, RPI = 32 / LPR, UNR = 8;
-        const int sub = lane / LPR, li = lane % LPR;
-        const T* mu_u = mu + (size_t)u * cmax * D + li * CPL;
-        const int step = nwarps * RPI;
-        uint4 qw[G], v[UNR];
+    // ---- 2. unsorted keys (N is a multiple of NT: every slot is written)
 #pragma unroll
-        for (int h = 0; h < G; ++h) qw[h] = *reinterpret_cast<const uint4*>(q + ((size_t)u * G + h) * D + li * CPL);
-        // rb is the same for every lane of the warp (the loop below holds
-        // full-warp shuffles); the row of a lane is rb + sub + i * step
-        int rb = warp * RPI;
-        auto load_rows = [&](int b) {
-#pragma unroll
-            for (int i = 0; i < UNR; ++i) {
-                const int r = b + sub + i * step;
-                v[i] = r < C ? *reinterpret_cast<const uint4*>(mu_u + (size_t)r * D) : make_uint4(0, 0, 0, 0);
-            }
-        };
-        load_rows(rb);
-        // sum of the g query heads for channels li*CPL .. +CPL
-        float qc[CPL];
-#pragma unroll
-        for (int c = 0; c < CPL; ++c) qc[c] = 0.f;
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            float f[CPL];
-            Vec<T>::unpack(qw[h], f);
-#pragma unroll
-            for (int c = 0; c < CPL; ++c) qc[c] += f[c];
-        }
-        for (; rb < C; rb += step * UNR) {
-#pragma unroll
-            for (int i = 0; i < UNR; ++i) {
-                float f[CPL];
-                Vec<T>::unpack(v[i], f);
-                float dot = 0.f;
-#pragma unroll
-                for (int c = 0; c < CPL; ++c) dot = fmaf(qc[c], f[c], dot);
-#pragma unroll
-                for (int o = LPR / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(FULL, dot, o);
-                const int r = rb + sub + i * step;
-                if (li == 0 && r < C) sk[r] = rank_key(dot, r);
-            }
-            if (rb + step * UNR < C) load_rows(rb + step * UNR);
-        }
-        for (int c = C + tid; c < N; c += NT) sk[c] = ~0ull;
+    for (int e = 0; e < E; ++e) {
+        const int c = e * NT + tid;
+        sk[c] = c < C ? rank_key(scr[e], c) : ~0ull;
     }
 #pragma unroll
     for (int e = 0; e < E; ++e) {
@@ -975,7 +933,7 @@ cudaError_t launch_attn_t(const void* q, const void* K, const void* V, const int
     if (a.ipu < 1) a.ipu = 1;
     if (a.ipu > max_splits) return cudaErrorInvalidValue;
     a.total = a.ipu * units;
-    int grid = num_sms > 0 ? num_sms : 148;
+    int grid = num_sms > 0 ? num_sms : 152;
     if (grid > a.total) grid = a.total;
     a.ipc = (a.total + grid - 1) / grid;
     // a unit spans at most 16 CTAs (the combine kernel's limit)
@@ -1001,14 +959,29 @@ cudaError_t launch_score_t(const void* q, const void* mu, int g, int units, int 
                            float* scores, int stride, cudaStream_t s) {
     constexpr int RPW = (32 / (D / Vec<T>::N)) * 4;  // rows per warp
     dim3 grid((C + 8 * RPW - 1) / (8 * RPW), units);
+#define CKV_SCORE(G)                                                                                     \
+    return launch_dependent(score_kernel<T, G>, grid, dim3(256), 0, s, (const T*)q, (const T*)mu, cmax, C, \
+                            scores, stride)
     switch (g) {
-        case 1: score_kernel<T, 1><<<grid, 256, 0, s>>>((const T*)q, (const T*)mu, cmax, C, scores, stride); break;
-        case 2: score_kernel<T, 2><<<grid, 256, 0, s>>>((const T*)q, (const T*)mu, cmax, C, scores, stride); break;
-        case 4: score_kernel<T, 4><<<grid, 256, 0, s>>>((const T*)q, (const T*)mu, cmax, C, scores, stride); break;
-        case 8: score_kernel<T, 8><<<grid, 256, 0, s>>>((const T*)q, (const T*)mu, cmax, C, scores, stride); break;
-        default: return cudaErrorInvalidValue;
+        case 1: CKV_SCORE(1);
+        case 2: CKV_SCORE(2);
+        case 4: CKV_SCORE(4);
+        case 8: CKV_SCORE(8);
     }
-    return cudaGetLastError();
+#undef CKV_SCORE
+    return cudaErrorInvalidValue;
+}
+
+template <int E>
+cudaError_t launch_sel_t(const ckv_ctx* ctx, const float* scores, int stride, int C, int N, int B, int32_t* idx,
+                         int32_t* count, cudaStream_t s) {
+    const size_t smem = (size_t)N * 24 + (size_t)4096 * 4;
+    auto kern = sel_kernel<E>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_dependent(kern, dim3(ctx->cfg.units), dim3(N / E), smem, s, scores, stride, ctx->cmax, C, N,
+                            (const int32_t*)ctx->sizes, (const int32_t*)ctx->offsets, (const int32_t*)ctx->perm,
+                            ctx->ntok, B, idx, count, ctx->dev_err);
 }
 
 }  // namespace
@@ -1023,50 +996,22 @@ cudaError_t launch_score(const ckv_ctx* ctx, const void* q, int C, float* scores
                                  stride, s);
 }
 
-template <typename T, int G, int E, bool FS>
-cudaError_t launch_sel_t(const ckv_ctx* ctx, const void* q, const float* scores, int stride, int C, int N,
-                         int B, int32_t* idx, int32_t* count, cudaStream_t s) {
-    const size_t smem = (size_t)N * 24 + (size_t)4096 * 4;
-    auto kern = sel_kernel<T, G, E, FS>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    return launch_dependent(kern, dim3(ctx->cfg.units), dim3(N / E), smem, s, (const T*)q, (const T*)ctx->mu_s,
-                            ctx->cmax, scores, stride, C, N, (const int32_t*)ctx->sizes,
-                            (const int32_t*)ctx->offsets, (const int32_t*)ctx->perm, ctx->ntok, B, idx, count,
-                            ctx->dev_err);
-}
-
-template <typename T, int E, bool FS>
-cudaError_t launch_sel_g(const ckv_ctx* ctx, const void* q, const float* scores, int stride, int C, int N, int B,
-                         int32_t* idx, int32_t* count, cudaStream_t s) {
-    switch (ctx->cfg.g) {
-        case 1: return launch_sel_t<T, 1, E, FS>(ctx, q, scores, stride, C, N, B, idx, count, s);
-        case 2: return launch_sel_t<T, 2, E, FS>(ctx, q, scores, stride, C, N, B, idx, count, s);
-        case 4: return launch_sel_t<T, 4, E, FS>(ctx, q, scores, stride, C, N, B, idx, count, s);
-        case 8: return launch_sel_t<T, 8, E, FS>(ctx, q, scores, stride, C, N, B, idx, count, s);
-    }
-    return cudaErrorInvalidValue;
-}
-
-template <typename T, bool FS>
-cudaError_t launch_sel_e(const ckv_ctx* ctx, const void* q, const float* scores, int stride, int C, int B,
-                         int32_t* idx, int32_t* count, cudaStream_t s) {
-    int N = 128;
-    while (N < C) N <<= 1;
-    if (N <= 1024) return launch_sel_g<T, 1, FS>(ctx, q, scores, stride, C, N, B, idx, count, s);
-    if (N == 2048) return launch_sel_g<T, 2, FS>(ctx, q, scores, stride, C, N, B, idx, count, s);
-    if (N == 4096) return launch_sel_g<T, 4, FS>(ctx, q, scores, stride, C, N, B, idx, count, s);
-    return cudaErrorInvalidValue;
-}
-
 cudaError_t launch_select(const ckv_ctx* ctx, const void* q, const float* scores, int stride, int C, int B,
                           int32_t* idx, int32_t* count, cudaStream_t s) {
-    const bool bf16 = ctx->cfg.kv_dtype == CKV_BF16;
-    if (scores)
-        return bf16 ? launch_sel_e<__nv_bfloat16, true>(ctx, nullptr, scores, stride, C, B, idx, count, s)
-                    : launch_sel_e<float, true>(ctx, nullptr, scores, stride, C, B, idx, count, s);
-    return bf16 ? launch_sel_e<__nv_bfloat16, false>(ctx, q, nullptr, 0, C, B, idx, count, s)
-                : launch_sel_e<float, false>(ctx, q, nullptr, 0, C, B, idx, count, s);
+    if (!scores) {
+        // scores of every cluster into the context's scratch (a many-CTA
+        // stream over the centroid table), then the selection reads them
+        cudaError_t e = launch_score(ctx, q, C, ctx->scores, ctx->cmax, s);
+        if (e != cudaSuccess) return e;
+        scores = ctx->scores;
+        stride = ctx->cmax;
+    }
+    int N = 128;
+    while (N < C) N <<= 1;
+    if (N <= 1024) return launch_sel_t<1>(ctx, scores, stride, C, N, B, idx, count, s);
+    if (N == 2048) return launch_sel_t<2>(ctx, scores, stride, C, N, B, idx, count, s);
+    if (N == 4096) return launch_sel_t<4>(ctx, scores, stride, C, N, B, idx, count, s);
+    return cudaErrorInvalidValue;
 }
 
 int attention_rows_per_split(int kv_dtype, int g) {
@@ -1094,7 +1039,7 @@ cudaError_t launch_attention(const void* q, const void* K, const void* V, const 
     if (kv_dtype == CKV_BF16) {
         // bf16 K/V: tensor-core kernel (attn_mma.cu); fp32 K/V: CUDA-core kernel below
         return launch_attention_mma(q, K, V, idx, count, units, g, max_len, sinks, clustered_end, cur_len, B,
-                                    out, part, counters, max_splits, dev_err, num_sms, s);
+                                    out, part, max_splits, dev_err, num_sms, s);
     } else {
         switch (g) {
             case 1: CKV_ATTN(float, 1);

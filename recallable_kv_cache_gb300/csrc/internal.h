@@ -104,6 +104,7 @@ cudaError_t launch_select(const ckv_ctx* ctx, const void* q, const float* scores
                           int32_t* idx, int32_t* count, cudaStream_t s);
 constexpr int MAX_SELECT_CLUSTERS = 4096;
 // split-K sparse decode attention; partials/counters are caller-provided scratch
+// (the counters serve the fp32 kernel's in-kernel combine only)
 cudaError_t launch_attention(const void* q, const void* K, const void* V, const int32_t* idx,
                              const int32_t* count, int units, int g, int kv_dtype, int max_len,
                              int sinks, int clustered_end, int cur_len, int B, float* out,
@@ -115,7 +116,7 @@ int attention_rows_per_split(int kv_dtype, int g);
 int attention_mma_rows_per_tile();
 cudaError_t launch_attention_mma(const void* q, const void* K, const void* V, const int32_t* idx,
                                  const int32_t* count, int units, int g, int max_len, int sinks, int clustered_end,
-                                 int cur_len, int B, float* out, float* part, int32_t* counters, int max_slots,
-                                 int32_t* dev_err, int num_sms, cudaStream_t s);
+                                 int cur_len, int B, float* out, float* part, int max_slots, int32_t* dev_err,
+                                 int num_sms, cudaStream_t s);
 
 }  // namespace ckv

@@ -74,7 +74,9 @@ def test_select_given_scores_bit_exact(case, B):
         assert (idx[u, wc:] == -7).all()  # entries past count untouched
 
 
-def test_fused_select_equals_score_then_select(case):
+def test_select_equals_score_then_select(case):
+    """ckv_select (scoring into the context's scratch, then selection) against
+    the two public calls ckv_score + ckv_select_scored."""
     w, ctx = case["w"], case["ctx"]
     q = case["Q"][1].cuda().contiguous()
     sc = torch.empty(w.units, w.C, dtype=torch.float32, device="cuda")
@@ -208,7 +210,7 @@ def test_select_large_cluster_counts(C):
             want, wc = ck.select(scores[u].astype(np.float64), st["sizes"], st["offsets"], st["perm"], B)
             assert cnt[u].item() == wc
             assert np.array_equal(idx[u, :wc].cpu().numpy(), want)
-    # fused path: its scores must rank like the GPU's own scores
+    # ckv_select: its scores must rank like the GPU's own scores
     q = torch.from_numpy(rng.standard_normal((U, 4, d))).to(torch.bfloat16).cuda()
     sc = torch.empty(U, C, dtype=torch.float32, device="cuda")
     ctx.score(q, sc)
@@ -217,7 +219,7 @@ def test_select_large_cluster_counts(C):
     i2, c2 = torch.empty_like(i1), torch.empty_like(c1)
     ctx.select_scored(sc, 2048, i1, c1)
     ctx.select(q, 2048, i2, c2)
-    # the fused kernel sums in the same order as ckv_score: identical selection
+    # ckv_select scores with the same kernel as ckv_score: identical selection
     assert torch.equal(c1, c2)
     for u in range(U):
         assert torch.equal(i1[u, :c1[u]], i2[u, :c2[u]])
