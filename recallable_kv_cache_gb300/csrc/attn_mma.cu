@@ -110,11 +110,20 @@ __global__ void __launch_bounds__(MW * 32, 1) attn_mma_kernel(const MmaArgs a) {
     const uint32_t wbase_addr = ptx::smem_u32(wbase);
     const int pend = a.cur_len - a.clustered_end;
 
-    // ---- token of row (lane & 15) of tile t, -1 if none (count cached per unit)
+    // ---- token of row (lane & 15) of tile t, -1 if none (count cached per unit).
+    // The idx entry is loaded before the count is known (any slot below B is
+    // a valid address) so that both loads share one round trip; rows at or
+    // past the count are discarded afterwards.
     int cu_ids = -1, r_ids = 0;
     auto ids_for = [&](int t) -> int {
         if (t >= t_end) return -1;
         const int u = t / a.tpu, k = t % a.tpu;
+        const int r = k * TR + (lane & 15);
+        const int j = r - a.sinks - pend;
+        int tok;
+        if (r < a.sinks) tok = r;
+        else if (j < 0) tok = a.clustered_end + (r - a.sinks);
+        else tok = j < a.B ? a.idx[(size_t)u * a.B + j] : -1;
         if (u != cu_ids) {
             int c = a.count[u];
             if (c < 0 || c > a.B) {
@@ -124,12 +133,7 @@ __global__ void __launch_bounds__(MW * 32, 1) attn_mma_kernel(const MmaArgs a) {
             r_ids = a.sinks + pend + c;
             cu_ids = u;
         }
-        const int r = k * TR + (lane & 15);
         if (r >= r_ids) return -1;
-        int tok;
-        if (r < a.sinks) tok = r;
-        else if (r < a.sinks + pend) tok = a.clustered_end + (r - a.sinks);
-        else tok = a.idx[(size_t)u * a.B + (r - a.sinks - pend)];
         if (tok < 0 || tok >= a.cur_len) {
             if (a.dev_err) atomicCAS(a.dev_err, 0, CKV_DEV_BAD_INDEX);
             tok = -1;
