@@ -37,15 +37,15 @@ METRIC = "sparse-decode tokens/s at 32k ctx, B=1024; K-means ms/layer; % of HBM 
 
 # DRAM bytes (read + write) of one attn_mma_kernel launch per algorithmic byte,
 # from one ncu capture of the current kernel on this workload (decode step 41:
-# 146.8 MB of DRAM traffic for 143.5 MB of algorithmic bytes).  The traffic of a
+# 146.9 MB of DRAM traffic for 143.5 MB of algorithmic bytes).  The traffic of a
 # launch is this ratio times its algorithmic bytes (both grow with the attended
 # rows).  Set to None whenever the kernel changes until it is captured again.
-ATTN_TRAFFIC_PER_ALG_BYTE = 146.848 / 143.525
+ATTN_TRAFFIC_PER_ALG_BYTE = 146.897 / 143.525
 # Same for the whole decode step (--path step); None: not captured as one unit.
 STEP_TRAFFIC_PER_ALG_BYTE = None
 STEP_TRAFFIC_SOURCE = "not captured for the whole step"
 ATTN_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch (decode step 41, "
-                       "146.8 MB for 143.5 MB algorithmic), scaled to the mean launch by algorithmic bytes")
+                       "146.9 MB for 143.5 MB algorithmic), scaled to the mean launch by algorithmic bytes")
 WORKLOAD = "decode_32k"
 
 
@@ -134,11 +134,25 @@ class ExternalEvents:
         self.rt = ctypes.CDLL(path or "libcudart.so")
         self.rt.cudaEventRecordWithFlags.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
         self.rt.cudaEventRecordWithFlags.restype = ctypes.c_int
+        self.rt.cudaMemcpy2DAsync.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_size_t,
+                                              ctypes.c_size_t, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p]
+        self.rt.cudaMemcpy2DAsync.restype = ctypes.c_int
 
     def record(self, ev: torch.cuda.Event, stream: torch.cuda.Stream):
         r = self.rt.cudaEventRecordWithFlags(ctypes.c_void_p(ev.cuda_event), ctypes.c_void_p(stream.cuda_stream), 1)
         if r != 0:
             raise RuntimeError(f"cudaEventRecordWithFlags failed: {r}")
+
+    def copy_rows_h2d(self, dst: torch.Tensor, src: torch.Tensor, stream: torch.cuda.Stream):
+        """src [n, w] contiguous pinned host -> dst [n, w] device view with a row
+        stride: one cudaMemcpy2DAsync (rows land where the caller's layout wants
+        them, no staging copy)."""
+        width = src.shape[1] * src.element_size()
+        r = self.rt.cudaMemcpy2DAsync(ctypes.c_void_p(dst.data_ptr()), ctypes.c_size_t(dst.stride(0) * dst.element_size()),
+                                      ctypes.c_void_p(src.data_ptr()), ctypes.c_size_t(width), ctypes.c_size_t(width),
+                                      ctypes.c_size_t(src.shape[0]), 1, ctypes.c_void_p(stream.cuda_stream))
+        if r != 0:
+            raise RuntimeError(f"cudaMemcpy2DAsync failed: {r}")
 
 
 # ----------------------------------------------------------------------------- algorithmic bytes
@@ -318,13 +332,14 @@ def run_ours(args, w, rank, world, device):
     res["decode_bytes_per_step"] = sum(decode_bytes(w, t, C_at[t], ai)[1] for t in range(T)) / T
     res["assign_ms"] = time_assign(ctx, w, K)
     res["recall"] = selection_recall(lambda q, i, c: ctx.select(q, w.B, i, c), w, K, Q)
+    res["reuse"] = selection_reuse(ctx, w)
     res["quest"] = quest_comparator(w, K, V, Q)
     res["full_kv"] = full_kv_attention(w, K, V, Q)
     res["w"] = w
     res["ctx"] = ctx
     res["tensors"] = (K, V, Q)
     if not args.no_e2e:
-        res["e2e"] = run_e2e(ctx, w, K, V, Q, one_call)
+        res["e2e"] = run_e2e(ctx, w, K, V, Q, one_call, args.sync_incremental)
     return res
 
 
@@ -371,6 +386,41 @@ def selection_recall(select, w, K, Q, units=(0, 97, 201), queries=(0, 1, 2), wha
             mass.append((a[sel].sum() / a[top].sum()).item())
     return {"token": statistics.mean(tok), "attention_mass": statistics.mean(mass),
             "sample": f"{len(units)} units x {len(queries)} queries, {what}, B={w.B}"}
+
+
+def selection_reuse(ctx, w, steps=64):
+    """Hit rate of a cache of the last R steps' selections (the ClusterKV
+    page's cluster-granular cache of selected KV; a measurement, not part of
+    the path): tokens of a step's selection already selected in one of the R
+    previous steps, over all tokens selected, for R = 1 and 2, on two query
+    streams of the same units: a new topic every step (the bench's stream)
+    and one topic held for the whole sample (fresh noise every step)."""
+    from recallable_kv_cache_gb300 import ckv
+    U, B = w.units, w.B
+    res = {}
+    for name, run in (("new_topic_every_step", 1), ("topic_held", steps)):
+        Qr = synth.make_queries(w, steps, device="cuda", topic_run=run)
+        hi = [torch.empty(U, B, dtype=torch.int32, device="cuda") for _ in range(steps)]
+        hc = [torch.empty(U, dtype=torch.int32, device="cuda") for _ in range(steps)]
+        for t in range(steps):
+            ctx.select(Qr[t], B, hi[t], hc[t])
+        hits = torch.empty(U, dtype=torch.int32, device="cuda")
+        rates = {}
+        for R in (1, 2):
+            hs, ns = 0, 0
+            for t in range(R, steps):
+                ckv.selection_overlap([(hi[t - r], hc[t - r]) for r in range(1, R + 1)], hi[t], hc[t], hits,
+                                      w.max_len)
+                hs += int(hits.sum())
+                ns += int(hc[t].sum())
+            rates[f"R{R}"] = hs / max(ns, 1)
+        res[name] = rates
+    sel_bytes = U * B * 2 * w.d * 2
+    res["offload_h2d_bytes_saved_per_step"] = {k: v["R1"] * sel_bytes for k, v in res.items()}
+    res["sample"] = f"{steps} decode steps x {U} units, clusters of the current state, B={B}"
+    res["on_gpu"] = ("no HBM bytes saved: every K/V row is resident and each selected row is read once either "
+                     "way; the hit rate prices the host-to-device bytes an offloaded cache would skip")
+    return res
 
 
 def quest_comparator(w, K, V, Q, steps=64):
@@ -467,55 +517,125 @@ def full_kv_attention(w, K, V, Q, reps=5):
             "what": "attention over all L tokens of every unit with the same kernel (idx = every prompt token)"}
 
 
-def run_e2e(ctx, w, K, V, Q, one_call=False):
+def run_e2e(ctx, w, K, V, Q, one_call=False, sync_incremental=False):
     """The same job through the public API from pinned host buffers: upload the
     prompt K/V, prefill clustering, then per decode step upload q and the new
-    K/V row of every unit, select, attend, and read the output back."""
-    U, L, B, T, d = w.units, w.L, w.B, w.decode_steps, w.d
+    K/V row of every unit, select, attend, and read the output back.  The calls
+    are recorded once into a CUDA graph, as a serving loop would, and the timed
+    region replays it: every copy and kernel of the job runs inside it.
+    Dependencies are those of a real decode loop: the V upload overlaps the
+    clustering (which reads K only) after K's; a step's q and new K and V rows
+    are copied in parallel when the step starts (the rows straight into the
+    caches by strided copies); its output is read back on a side stream while
+    the next step runs (two output buffers)."""
+    U, L, B, T, d, g = w.units, w.L, w.B, w.decode_steps, w.d, w.g
     Kh = torch.empty(U, w.max_len, d, dtype=K.dtype, pin_memory=True)
     Vh = torch.empty_like(Kh, pin_memory=True)
     Kh.copy_(K)
     Vh.copy_(V)
-    Qh = torch.empty(Q.shape, dtype=Q.dtype, pin_memory=True)
-    Qh.copy_(Q)
-    knew = Kh[:, L:].transpose(0, 1).contiguous().pin_memory()   # [T, U, d]
-    vnew = Vh[:, L:].transpose(0, 1).contiguous().pin_memory()
-    outh = torch.empty(T, U, w.g, d, dtype=torch.float32, pin_memory=True)
+    # per step, one packed host record: q [U, g, d] | new K row [U, d] | new V row [U, d]
+    nq, nr = U * g * d, U * d
+    inp_h = torch.empty(T, nq + 2 * nr, dtype=K.dtype, pin_memory=True)
+    inp_h[:, :nq].copy_(Q[:T].reshape(T, nq))
+    inp_h[:, nq:nq + nr].copy_(K[:, L:L + T].transpose(0, 1).reshape(T, nr))
+    inp_h[:, nq + nr:].copy_(V[:, L:L + T].transpose(0, 1).reshape(T, nr))
+    outh = torch.empty(T, U, g, d, dtype=torch.float32, pin_memory=True)
     Kd = torch.empty_like(K)
     Vd = torch.empty_like(V)
-    qd = torch.empty(U, w.g, d, dtype=Q.dtype, device="cuda")
+    qd = torch.empty(U, g, d, dtype=Q.dtype, device="cuda")
     idx = torch.empty(U, B, dtype=torch.int32, device="cuda")
     cnt = torch.empty(U, dtype=torch.int32, device="cuda")
-    out = torch.empty(U, w.g, d, dtype=torch.float32, device="cuda")
+    outs = [torch.empty(U, g, d, dtype=torch.float32, device="cuda") for _ in range(2)]
+    s, side, up, dn, sk, sv = (torch.cuda.Stream() for _ in range(6))
+    e_fork, e_v = torch.cuda.Event(), torch.cuda.Event()
+    e_step = [torch.cuda.Event() for _ in range(T)]
+    e_k = [torch.cuda.Event() for _ in range(T)]
+    e_vr = [torch.cuda.Event() for _ in range(T)]
+    e_out = [torch.cuda.Event() for _ in range(T)]
+    e_read = [torch.cuda.Event() for _ in range(T)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for e in ev:  # torch creates the CUDA event on first record
+        e.record(s)
+    ext = ExternalEvents()  # captured records become timing nodes
     torch.cuda.synchronize()
 
     def job():
+        ext.record(ev[0], s)
         for u in range(U):
             Kd[u, :L].copy_(Kh[u, :L], non_blocking=True)
-            Vd[u, :L].copy_(Vh[u, :L], non_blocking=True)
+        ext.record(ev[1], s)
+        # V is not read before the first decode step: its upload follows K's
+        # (the two would share the link) and overlaps the clustering
+        e_fork.record(s)
+        up.wait_event(e_fork)
+        with torch.cuda.stream(up):
+            for u in range(U):
+                Vd[u, :L].copy_(Vh[u, :L], non_blocking=True)
+            e_v.record(up)
         ctx.cluster_prefill(Kd, L, w.C)
+        ext.record(ev[2], s)
+        s.wait_event(e_v)
+        commit_at = -1
         for t in range(T):
+            # the step's three inputs in parallel: q, and the new K and V rows
+            # straight into their place in the caches (one strided copy each)
+            e_step[t].record(s)
+            sk.wait_event(e_step[t])
+            ext.copy_rows_h2d(Kd[:, L + t], inp_h[t, nq:nq + nr].view(U, d), sk)
+            e_k[t].record(sk)
+            sv.wait_event(e_step[t])
+            ext.copy_rows_h2d(Vd[:, L + t], inp_h[t, nq + nr:].view(U, d), sv)
+            e_vr[t].record(sv)
+            qd.view(-1).copy_(inp_h[t, :nq], non_blocking=True)
+            s.wait_event(e_k[t])
+            s.wait_event(e_vr[t])
             if t > 0 and t % w.m == 0:
-                ctx.cluster_incremental(Kd, L + t - w.m)
-            qd.copy_(Qh[t], non_blocking=True)
-            Kd[:, L + t].copy_(knew[t], non_blocking=True)
-            Vd[:, L + t].copy_(vnew[t], non_blocking=True)
+                if sync_incremental:
+                    ctx.cluster_incremental(Kd, L + t - w.m)
+                else:
+                    e_fork.record(s)
+                    side.wait_event(e_fork)
+                    ctx.cluster_incremental_begin(Kd, L + t - w.m, stream=side)
+                    commit_at = t + 1
+            if t == commit_at:
+                ctx.cluster_incremental_commit(stream=s)
+            out = outs[t % 2]
+            if t >= 2:
+                s.wait_event(e_read[t - 2])  # that buffer's read-back is done
             if one_call:
                 ctx.decode_step(qd, Kd, Vd, B, L + t + 1, idx, cnt, out)
             else:
                 ctx.select(qd, B, idx, cnt)
                 ctx.sparse_decode_attn(qd, Kd, Vd, idx, cnt, B, L + t + 1, out)
-            outh[t].copy_(out, non_blocking=True)
-        torch.cuda.synchronize()
+            e_out[t].record(s)
+            dn.wait_event(e_out[t])
+            with torch.cuda.stream(dn):
+                outh[t].copy_(out, non_blocking=True)
+                e_read[t].record(dn)
+        s.wait_event(e_read[T - 1])
+        ext.record(ev[3], s)
 
-    job()  # warm-up
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            job()
+        graph.replay()  # warm-up
+    torch.cuda.synchronize()
     t0 = time.perf_counter()
-    job()
+    with torch.cuda.stream(s):
+        graph.replay()
+    torch.cuda.synchronize()
     dt = time.perf_counter() - t0
-    h2d = 2 * U * L * d * 2 + T * (U * w.g * d * 2 + 2 * U * d * 2)
-    d2h = T * U * w.g * d * 4
+    phases = {"upload_k_ms": ev[0].elapsed_time(ev[1]), "prefill_ms": ev[1].elapsed_time(ev[2]),
+              "decode_ms": ev[2].elapsed_time(ev[3])}
+    h2d = 2 * U * L * d * 2 + T * (nq + 2 * nr) * 2
+    d2h = T * U * g * d * 4
     return {"value": T / dt, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "job_s": dt}
+            "job_s": dt, "phases_ms": {k: round(v, 3) for k, v in phases.items()},
+            "how": "public API calls recorded once into a CUDA graph and replayed; the prompt K/V, every "
+                   "step's q and new K/V rows come from pinned host memory and every step's output goes "
+                   "back to it inside the timed replay (V upload overlapping the clustering, the step's three "
+                   "input copies in parallel, outputs read back while the next step runs)"}
 
 
 # ----------------------------------------------------------------------------- the oracle on the CPU
@@ -677,6 +797,7 @@ def main():
                             "frac": assign_flops / (r["assign_ms"] / 1000.0) / 1e12 / meas.get("bf16_tflops", 1900.0),
                             "launch_us": 1000.0 * r["assign_ms"], "peak_kind": peak_kind + " (burst: timed alone)"},
         "recall": r["recall"],
+        "reuse": r["reuse"],
         "full_kv": dict(r["full_kv"], decode_speedup=r["full_kv"]["attention_us"] / (1000.0 * decode_ms / T)),
         "quest": r["quest"],
         "phase_ms": {"prefill_clustering": prefill_ms, "decode_loop": decode_ms},

@@ -238,6 +238,27 @@ ckv_status ckv_quest_pages(const void* K, int32_t kv_dtype, int32_t units, int32
 ckv_status ckv_quest_score(const void* q, int32_t q_dtype, const void* page_max, const void* page_min,
                            int32_t units, int32_t g, int32_t n_pages, float* scores, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Reuse of earlier selections (section "Caching the KV of selected tokens":
+ * a cache of the KV selected in the last R decode steps, only clusters missing
+ * from it are loaded; cache-effectiveness analysis, hit rates for R = 1, 2).
+ *
+ * For every unit u: hits[u] = the number of tokens idx_cur[u][p],
+ * p < cnt_cur[u], that appear in at least one of the R previous selections
+ * idx_prev[r][u][0 .. cnt_prev[r][u]).  Whole clusters are selected, so
+ * hits[u] / cnt_cur[u] is the token-weighted cluster hit rate.  Nothing is
+ * loaded: every K/V row is resident, so this is a measurement only.
+ * idx_prev / cnt_prev are HOST arrays of R device pointers (idx [units][B_prev]
+ * int32, cnt [units] int32); idx_cur [units][B_cur], cnt_cur [units] and hits
+ * [units] are device pointers.  Counts are clamped to [0, B]; ids outside
+ * [0, max_len) are ignored.  R = 0 gives hits = 0.
+ * Errors: CKV_ERR_ARG (R outside [0, 8], null pointers, negative sizes),
+ * CKV_ERR_CAPACITY (max_len above 1.6 M tokens: the bitmap is in shared
+ * memory), CKV_ERR_CUDA. */
+ckv_status ckv_selection_overlap(int32_t units, int32_t max_len, int32_t R, const int32_t* const* idx_prev,
+                                 const int32_t* const* cnt_prev, int32_t B_prev, const int32_t* idx_cur,
+                                 const int32_t* cnt_cur, int32_t B_cur, int32_t* hits, void* stream);
+
 /* Sparse decode attention that allocates nothing and needs no context.
  * The ClusterKV paper has no counterpart of this call; it exists for callers
  * that cannot allocate device memory: code running while a CUDA graph is

@@ -35,6 +35,7 @@ SIGNATURES = {
     "ckv_decode_step": ([_P, _P, _I, _P, _P, _I, _I, _P, _P, _P, _P], _I),
     "ckv_quest_pages": ([_P, _I, _I, _I, _I, _I, _P, _P, _P], _I),
     "ckv_quest_score": ([_P, _I, _P, _P, _I, _I, _I, _P, _P], _I),
+    "ckv_selection_overlap": ([_I, _I, _I, _P, _P, _I, _P, _P, _I, _P, _P], _I),
     "ckv_cluster_incremental_begin": ([_P, _P, _I, _I, _I, _P], _I),
     "ckv_cluster_incremental_commit": ([_P, _P], _I),
     "ckv_get_info": ([_P, _P], _I),
@@ -239,3 +240,16 @@ def quest_score(q, page_max, page_min, scores, stream=None):
     units, g = q.shape[0], q.shape[1]
     _check(lib().ckv_quest_score(ptr(q), _dtype_code(q), ptr(page_max), ptr(page_min), units, g,
                                  page_max.shape[1], ptr(scores), _stream(stream)), "ckv_quest_score")
+
+
+def selection_overlap(prev, idx, count, hits, max_len: int, stream=None):
+    """hits[u] = tokens of the selection (idx, count) that appear in any of the
+    earlier selections ``prev`` = [(idx_r, count_r), ...] (see
+    ckv_selection_overlap).  All idx_r share one shape [units, B_prev]."""
+    units, B = idx.shape
+    R = len(prev)
+    B_prev = prev[0][0].shape[1] if R else 0
+    ip = (ctypes.c_void_p * max(R, 1))(*[ptr(p[0]) for p in prev])
+    cp = (ctypes.c_void_p * max(R, 1))(*[ptr(p[1]) for p in prev])
+    _check(lib().ckv_selection_overlap(units, max_len, R, ip, cp, B_prev, ptr(idx), ptr(count), B, ptr(hits),
+                                       _stream(stream)), "ckv_selection_overlap")

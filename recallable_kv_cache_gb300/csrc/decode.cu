@@ -54,6 +54,8 @@ __device__ __forceinline__ void set_err(int32_t* err, int32_t code) {
 // ============================================================================
 // scoring: scores[u][c] = sum_h q_h . mu_c = (sum_h q_h) . mu_c
 // ============================================================================
+constexpr int SCORE_UNROLL = 4;  // centroid rows in flight per lane group
+
 template <typename T, int G>
 __global__ void __launch_bounds__(256) score_kernel(const T* __restrict__ q,
                                                    const T* __restrict__ mu, int cmax, int C,
@@ -61,7 +63,7 @@ __global__ void __launch_bounds__(256) score_kernel(const T* __restrict__ q,
     constexpr int CPL = Vec<T>::N;   // channels per lane
     constexpr int LPR = D / CPL;     // lanes per centroid row
     constexpr int RPI = 32 / LPR;    // rows per warp-wide load
-    constexpr int UNROLL = 4;
+    constexpr int UNROLL = SCORE_UNROLL;
     const int u = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int sub = lane / LPR, li = lane % LPR;
@@ -957,7 +959,7 @@ cudaError_t launch_attn_t(const void* q, const void* K, const void* V, const int
 template <typename T>
 cudaError_t launch_score_t(const void* q, const void* mu, int g, int units, int cmax, int C,
                            float* scores, int stride, cudaStream_t s) {
-    constexpr int RPW = (32 / (D / Vec<T>::N)) * 4;  // rows per warp
+    constexpr int RPW = (32 / (D / Vec<T>::N)) * SCORE_UNROLL;  // rows per warp
     dim3 grid((C + 8 * RPW - 1) / (8 * RPW), units);
 #define CKV_SCORE(G)                                                                                     \
     return launch_dependent(score_kernel<T, G>, grid, dim3(256), 0, s, (const T*)q, (const T*)mu, cmax, C, \

@@ -147,12 +147,16 @@ def unit_values(w: Workload, unit: int, device="cpu") -> torch.Tensor:
     return v.to(w.torch_dtype())
 
 
-def unit_queries(w: Workload, unit: int, n: int, device="cpu", structure=None) -> torch.Tensor:
+def unit_queries(w: Workload, unit: int, n: int, device="cpu", structure=None, topic_run: int = 1) -> torch.Tensor:
     """``n`` query groups [n, g, d] of one unit: every group picks one random
-    centre j and its g heads are q_h = q_scale * c_j + q_sigma * noise."""
+    centre j and its g heads are q_h = q_scale * c_j + q_sigma * noise.  With
+    topic_run > 1 each drawn centre is kept for topic_run consecutive groups
+    (fresh noise every group)."""
     c, _, _ = structure if structure is not None else unit_structure(w, unit, device)
     g = _gen(w, "queries", unit, device)
     j = torch.randint(0, w.n_centres, (n,), generator=g, device=device)
+    if topic_run > 1:
+        j = j[(torch.arange(n, device=device) // topic_run) * topic_run]
     noise = torch.randn(n, w.g, w.d, generator=g, device=device, dtype=torch.float32)
     q = c[j][:, None, :] * w.q_scale + noise * w.q_sigma
     return q.to(w.torch_dtype())
@@ -171,10 +175,11 @@ def make_kv(w: Workload, units=None, device="cpu"):
     return K, V
 
 
-def make_queries(w: Workload, n: int, units=None, device="cpu") -> torch.Tensor:
-    """Queries [n, len(units), g, d]: ``n`` independent query groups per unit."""
+def make_queries(w: Workload, n: int, units=None, device="cpu", topic_run: int = 1) -> torch.Tensor:
+    """Queries [n, len(units), g, d]: ``n`` query groups per unit (a new random
+    centre every group, or every topic_run groups)."""
     units = list(range(w.units) if units is None else units)
     Q = torch.empty(n, len(units), w.g, w.d, dtype=w.torch_dtype(), device=device)
     for i, u in enumerate(units):
-        Q[:, i] = unit_queries(w, u, n, device)
+        Q[:, i] = unit_queries(w, u, n, device, topic_run=topic_run)
     return Q
