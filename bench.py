@@ -334,6 +334,7 @@ def run_ours(args, w, rank, world, device):
     res["recall"] = selection_recall(lambda q, i, c: ctx.select(q, w.B, i, c), w, K, Q)
     res["reuse"] = selection_reuse(ctx, w)
     res["quest"] = quest_comparator(w, K, V, Q)
+    res["channel_prescore"] = channel_prescore_comparator(w, K, Q)
     res["full_kv"] = full_kv_attention(w, K, V, Q)
     res["w"] = w
     res["ctx"] = ctx
@@ -482,6 +483,64 @@ def quest_comparator(w, K, V, Q, steps=64):
             "metadata_bytes_per_step": U * P * 2 * w.d * K.element_size(),
             "what": "Quest-style pages of 16 tokens: per-channel max / min keys, weight = upper bound of q.k "
                     "summed over the heads; whole pages up to B; same attention kernel; one pending token"}
+
+
+def channel_prescore_comparator(w, K, Q, steps=64, rs=(8, 16)):
+    """TailorKV-style channel pre-score as the centroid scorer (an alternative
+    cheap scorer, a comparator): the same prefill clusters, per step the r
+    critical channels of |sum_h q_h| * max_c |mu_c| and the scores over them,
+    then the same cluster selection.  Reports the selection time per step
+    (scoring + selection, a graph of `steps` steps) beside the exact scorer's,
+    and the recall of each, measured like the main recall."""
+    from recallable_kv_cache_gb300 import ckv
+    U, L, B = w.units, w.L, w.B
+    tctx = ckv.Context(units=U, g=w.g, max_len=w.max_len, max_clusters=w.max_clusters, max_budget=B,
+                       iters=w.iters, m=w.m, c_plus=w.c_plus)
+    tctx.cluster_prefill(K, L, w.C)
+    muT = torch.empty(U, w.d, w.max_clusters, dtype=K.dtype, device="cuda")
+    chmax = torch.empty(U, w.d, dtype=torch.float32, device="cuda")
+    tctx.centroid_channels(muT, chmax)
+    scores = torch.empty(U, w.C, dtype=torch.float32, device="cuda")
+    idx = torch.empty(U, B, dtype=torch.int32, device="cuda")
+    cnt = torch.empty(U, dtype=torch.int32, device="cuda")
+    s = torch.cuda.Stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timed(select):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            for t in range(2):
+                select(Q[t], idx, cnt)
+            with torch.cuda.graph(g, stream=s):
+                for t in range(steps):
+                    select(Q[t], idx, cnt)
+            g.replay()
+            e0.record(s)
+            for _ in range(3):
+                g.replay()
+            e1.record(s)
+        torch.cuda.synchronize()
+        return 1000.0 * e0.elapsed_time(e1) / (3 * steps)
+
+    exact = lambda q, i, c: tctx.select(q, B, i, c)
+    res = {"exact": {"select_us": timed(exact),
+                     "recall": selection_recall(exact, w, K, Q, what="exact centroid scores")}}
+    for r in rs:
+        def pre(q, i, c, r=r):
+            tctx.channel_prescore(q, muT, chmax, r, scores)
+            tctx.select_scored(scores, B, i, c)
+        res[f"r{r}"] = {"select_us": timed(pre),
+                        "recall": selection_recall(pre, w, K, Q, what=f"{r} critical channels"),
+                        "centroid_bytes_per_step": U * r * w.C * K.element_size()}
+    e0.record()
+    tctx.centroid_channels(muT, chmax)
+    e1.record()
+    torch.cuda.synchronize()
+    res["channel_copy_ms"] = e0.elapsed_time(e1)
+    res["what"] = ("scores over the r channels of largest |sum_h q_h,i| * max_c |mu_c,i| from a channel-major "
+                   "centroid copy (rebuilt when the clusters change), then the same selection")
+    tctx.close()
+    return res
 
 
 def full_kv_attention(w, K, V, Q, reps=5):
@@ -798,6 +857,7 @@ def main():
                             "launch_us": 1000.0 * r["assign_ms"], "peak_kind": peak_kind + " (burst: timed alone)"},
         "recall": r["recall"],
         "reuse": r["reuse"],
+        "channel_prescore": r["channel_prescore"],
         "full_kv": dict(r["full_kv"], decode_speedup=r["full_kv"]["attention_us"] / (1000.0 * decode_ms / T)),
         "quest": r["quest"],
         "phase_ms": {"prefill_clustering": prefill_ms, "decode_loop": decode_ms},

@@ -259,6 +259,30 @@ ckv_status ckv_selection_overlap(int32_t units, int32_t max_len, int32_t R, cons
                                  const int32_t* const* cnt_prev, int32_t B_prev, const int32_t* idx_cur,
                                  const int32_t* cnt_cur, int32_t B_cur, int32_t* hits, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Channel pre-score, an alternative cheap scorer over the centroid table after
+ * TailorKV's channel contribution (TailorKV page, dynamic retrieval for
+ * sparsity-friendly layers: s_i = |q_i| * max |K_i|; attention scores
+ * approximated from the critical channels only).
+ *
+ * ckv_centroid_channels writes a channel-major copy of the context's scoring
+ * centroids, muT [units][d][max_clusters] of kv_dtype (entries c < n_clusters
+ * written), and chmax [units][d] float = max over the current clusters of
+ * |mu_c,i|.  Rebuild both whenever the clusters change (prefill, incremental
+ * commit, import).  Caller-owned, 16-byte aligned.
+ *
+ * ckv_channel_prescore, per unit: qs_i = sum_h q_h,i (fp32, heads in order),
+ * s_i = |qs_i| * chmax_i (fp32); the r channels of largest s_i (ties: lower
+ * channel) in descending order ch_0 .. ch_{r-1}; then for every current
+ * cluster scores[u][c] = sum_{j<r} qs_{ch_j} * muT[u][ch_j][c] (fp32, j in
+ * order), row stride n_clusters like ckv_score, ready for ckv_select_scored.
+ * channels [units][r] int32 receives ch_j when not null.  r in [1, 32].
+ * Errors: CKV_ERR_ARG, CKV_ERR_DTYPE (q_dtype != kv_dtype), CKV_ERR_ALIGN,
+ * CKV_ERR_STATE (no clusters). */
+ckv_status ckv_centroid_channels(ckv_ctx* ctx, void* muT, float* chmax, void* stream);
+ckv_status ckv_channel_prescore(ckv_ctx* ctx, const void* q, int32_t q_dtype, const void* muT, const float* chmax,
+                                int32_t r, float* scores, int32_t* channels, void* stream);
+
 /* Sparse decode attention that allocates nothing and needs no context.
  * The ClusterKV paper has no counterpart of this call; it exists for callers
  * that cannot allocate device memory: code running while a CUDA graph is

@@ -36,6 +36,8 @@ SIGNATURES = {
     "ckv_quest_pages": ([_P, _I, _I, _I, _I, _I, _P, _P, _P], _I),
     "ckv_quest_score": ([_P, _I, _P, _P, _I, _I, _I, _P, _P], _I),
     "ckv_selection_overlap": ([_I, _I, _I, _P, _P, _I, _P, _P, _I, _P, _P], _I),
+    "ckv_centroid_channels": ([_P, _P, _P, _P], _I),
+    "ckv_channel_prescore": ([_P, _P, _I, _P, _P, _I, _P, _P, _P], _I),
     "ckv_cluster_incremental_begin": ([_P, _P, _I, _I, _I, _P], _I),
     "ckv_cluster_incremental_commit": ([_P, _P], _I),
     "ckv_get_info": ([_P, _P], _I),
@@ -175,6 +177,16 @@ class Context:
     def score(self, q, scores, stream=None):
         _check(lib().ckv_score(self.handle, ptr(q), _dtype_code(q), ptr(scores), _stream(stream)),
                "ckv_score")
+
+    def centroid_channels(self, muT, chmax, stream=None):
+        """Channel-major scoring centroids and per-channel maxima (see ckv_centroid_channels)."""
+        _check(lib().ckv_centroid_channels(self.handle, ptr(muT), ptr(chmax), _stream(stream)),
+               "ckv_centroid_channels")
+
+    def channel_prescore(self, q, muT, chmax, r: int, scores, channels=None, stream=None):
+        """Scores over the r critical channels (see ckv_channel_prescore)."""
+        _check(lib().ckv_channel_prescore(self.handle, ptr(q), _dtype_code(q), ptr(muT), ptr(chmax), r,
+                                          ptr(scores), ptr(channels), _stream(stream)), "ckv_channel_prescore")
 
     def select_scored(self, scores, B: int, idx, count, stream=None):
         _check(lib().ckv_select_scored(self.handle, ptr(scores), B, ptr(idx), ptr(count),
