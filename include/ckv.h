@@ -20,7 +20,11 @@
  *             clustered; always attended.
  *
  * Buffers (all pointers are DEVICE pointers unless stated, 16-byte aligned,
- * row-contiguous, owned by the caller; the library never frees them):
+ * row-contiguous, owned by the caller; the library never frees them).  A
+ * device pointer is any address the kernels can access: device memory, or
+ * pinned host memory the device maps (with unified addressing its host
+ * address), for the small per-step inputs and outputs (q, out, the appended
+ * K/V rows), which then cross the host link inside the kernels:
  *   K, V      [units][max_len][d] of kv_dtype.  Row t of unit u starts at
  *             element (u * max_len + t) * d.
  *   q         [units][g][d] of kv_dtype (q_dtype must equal kv_dtype).
@@ -195,6 +199,17 @@ ckv_status ckv_select_scored(ckv_ctx* ctx, const float* scores, int32_t B, int32
 /* ckv_score followed by ckv_select_scored (scores kept in the workspace). */
 ckv_status ckv_select(ckv_ctx* ctx, const void* q, int32_t q_dtype, int32_t B, int32_t* idx,
                       int32_t* count, void* stream);
+
+/* Appends one decode step's keys and values to the caches (section
+ * "Clustering in semantic space", clustering strategy during inference: a
+ * generated token's K/V join the cache and stay pending until their block is
+ * clustered).  For every unit u: K[u][pos][:] = k_new[u][:] and
+ * V[u][pos][:] = v_new[u][:]; k_new, v_new [units][d] of kv_dtype.  Does not
+ * touch any context: the attention calls see the rows through cur_len.
+ * Errors: CKV_ERR_ARG (pos outside [0, max_len)), CKV_ERR_DTYPE,
+ * CKV_ERR_ALIGN. */
+ckv_status ckv_append_kv(const void* k_new, const void* v_new, int32_t kv_dtype, int32_t units, int32_t max_len,
+                         int32_t pos, void* K, void* V, void* stream);
 
 /* Sparse decode attention (section "Background": softmax(q K_S^T / sqrt(d))
  * V_S).  For every unit and query head h: o_h = softmax over the attended

@@ -37,6 +37,7 @@ SIGNATURES = {
     "ckv_quest_score": ([_P, _I, _P, _P, _I, _I, _I, _P, _P], _I),
     "ckv_selection_overlap": ([_I, _I, _I, _P, _P, _I, _P, _P, _I, _P, _P], _I),
     "ckv_centroid_channels": ([_P, _P, _P, _P], _I),
+    "ckv_append_kv": ([_P, _P, _I, _I, _I, _I, _P, _P, _P], _I),
     "ckv_channel_prescore": ([_P, _P, _I, _P, _P, _I, _P, _P, _P], _I),
     "ckv_cluster_incremental_begin": ([_P, _P, _I, _I, _I, _P], _I),
     "ckv_cluster_incremental_commit": ([_P, _P], _I),
@@ -265,3 +266,11 @@ def selection_overlap(prev, idx, count, hits, max_len: int, stream=None):
     cp = (ctypes.c_void_p * max(R, 1))(*[ptr(p[1]) for p in prev])
     _check(lib().ckv_selection_overlap(units, max_len, R, ip, cp, B_prev, ptr(idx), ptr(count), B, ptr(hits),
                                        _stream(stream)), "ckv_selection_overlap")
+
+
+def append_kv(k_new, v_new, K, V, pos: int, stream=None):
+    """Row ``pos`` of every unit of K and V := k_new[u], v_new[u] (see ckv_append_kv).
+    k_new / v_new may live in pinned host memory the device maps."""
+    units, max_len = K.shape[0], K.shape[1]
+    _check(lib().ckv_append_kv(ptr(k_new), ptr(v_new), _dtype_code(K), units, max_len, pos, ptr(K), ptr(V),
+                               _stream(stream)), "ckv_append_kv")

@@ -108,3 +108,20 @@ def export_state(ctx: ckv.Context, units: int, d: int = 128, dtype: str = "bf16"
     return dict(mu=mu.cpu().numpy().astype(np.float64), mu_hat=mh.float().cpu().numpy(),
                 sizes=sizes.cpu().numpy(), offsets=offs.cpu().numpy(),
                 perm=perm.cpu().numpy()[:, :np_])
+
+
+def host_mapped(t: torch.Tensor) -> bool:
+    """True when the pinned host tensor t is addressable by kernels at its host
+    address (unified addressing); checked with cudaHostGetDevicePointer."""
+    import ctypes
+    path = None
+    for line in open("/proc/self/maps"):
+        if "libcudart" in line:
+            path = line.split()[-1]
+            break
+    rt = ctypes.CDLL(path or "libcudart.so")
+    rt.cudaHostGetDevicePointer.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_void_p, ctypes.c_uint]
+    rt.cudaHostGetDevicePointer.restype = ctypes.c_int
+    d = ctypes.c_void_p()
+    return rt.cudaHostGetDevicePointer(ctypes.byref(d), ctypes.c_void_p(t.data_ptr()), 0) == 0 and \
+        d.value == t.data_ptr()
