@@ -153,6 +153,18 @@ class ExternalEvents:
         r = self.rt.cudaHostGetDevicePointer(ctypes.byref(dptr), ctypes.c_void_p(t.data_ptr()), 0)
         return r == 0 and dptr.value == t.data_ptr()
 
+    def copy_prefix_h2d(self, dst: torch.Tensor, src: torch.Tensor, rows: int, stream: torch.cuda.Stream):
+        """Rows [0, rows) of every unit of src [units, max_len, d] (pinned host)
+        into dst (same shape, device): one cudaMemcpy2DAsync (a little faster
+        than one copy per unit; the host link runs at ~211 GB/s either way)."""
+        pitch = src.stride(0) * src.element_size()
+        r = self.rt.cudaMemcpy2DAsync(ctypes.c_void_p(dst.data_ptr()), ctypes.c_size_t(dst.stride(0) * dst.element_size()),
+                                      ctypes.c_void_p(src.data_ptr()), ctypes.c_size_t(pitch),
+                                      ctypes.c_size_t(rows * src.stride(1) * src.element_size()),
+                                      ctypes.c_size_t(src.shape[0]), 1, ctypes.c_void_p(stream.cuda_stream))
+        if r != 0:
+            raise RuntimeError(f"cudaMemcpy2DAsync failed: {r}")
+
     def copy_rows_h2d(self, dst: torch.Tensor, src: torch.Tensor, stream: torch.cuda.Stream):
         """src [n, w] contiguous pinned host -> dst [n, w] device view with a row
         stride: one cudaMemcpy2DAsync (rows land where the caller's layout wants
@@ -637,17 +649,14 @@ def run_e2e(ctx, w, K, V, Q, one_call=False, sync_incremental=False):
 
     def job():
         ext.record(ev[0], s)
-        for u in range(U):
-            Kd[u, :L].copy_(Kh[u, :L], non_blocking=True)
+        ext.copy_prefix_h2d(Kd, Kh, L, s)
         ext.record(ev[1], s)
         # V is not read before the first decode step: its upload follows K's
         # (the two would share the link) and overlaps the clustering
         e_fork.record(s)
         up.wait_event(e_fork)
-        with torch.cuda.stream(up):
-            for u in range(U):
-                Vd[u, :L].copy_(Vh[u, :L], non_blocking=True)
-            e_v.record(up)
+        ext.copy_prefix_h2d(Vd, Vh, L, up)
+        e_v.record(up)
         ctx.cluster_prefill(Kd, L, w.C)
         ext.record(ev[2], s)
         s.wait_event(e_v)

@@ -200,16 +200,19 @@ ckv_status ckv_select_scored(ckv_ctx* ctx, const float* scores, int32_t B, int32
 ckv_status ckv_select(ckv_ctx* ctx, const void* q, int32_t q_dtype, int32_t B, int32_t* idx,
                       int32_t* count, void* stream);
 
-/* Appends one decode step's keys and values to the caches (section
- * "Clustering in semantic space", clustering strategy during inference: a
- * generated token's K/V join the cache and stay pending until their block is
- * clustered).  For every unit u: K[u][pos][:] = k_new[u][:] and
- * V[u][pos][:] = v_new[u][:]; k_new, v_new [units][d] of kv_dtype.  Does not
- * touch any context: the attention calls see the rows through cur_len.
- * Errors: CKV_ERR_ARG (pos outside [0, max_len)), CKV_ERR_DTYPE,
- * CKV_ERR_ALIGN. */
-ckv_status ckv_append_kv(const void* k_new, const void* v_new, int32_t kv_dtype, int32_t units, int32_t max_len,
-                         int32_t pos, void* K, void* V, void* stream);
+/* Appends keys and values to the caches (section "Clustering in semantic
+ * space", clustering strategy during inference: a generated token's K/V join
+ * the cache and stay pending until their block is clustered; the prompt's K/V
+ * are the cache the prefill clustering reads).  For every unit u and row
+ * j < n: K[u][pos + j][:] = k_src[u][j][:] and V[u][pos + j][:] =
+ * v_src[u][j][:]; k_src, v_src [units][src_len][d] of kv_dtype (src_len >= n
+ * rows per unit; n = 1, src_len = 1 for one decode step).  The copy runs on
+ * the SMs, so the sources may be mapped pinned host memory.  Touches no
+ * context: the attention calls see the rows through cur_len.
+ * Errors: CKV_ERR_ARG (n < 1, src_len < n, [pos, pos + n) outside
+ * [0, max_len)), CKV_ERR_DTYPE, CKV_ERR_ALIGN. */
+ckv_status ckv_append_kv(const void* k_src, const void* v_src, int32_t src_len, int32_t kv_dtype, int32_t units,
+                         int32_t max_len, int32_t pos, int32_t n, void* K, void* V, void* stream);
 
 /* Sparse decode attention (section "Background": softmax(q K_S^T / sqrt(d))
  * V_S).  For every unit and query head h: o_h = softmax over the attended

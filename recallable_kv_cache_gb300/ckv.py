@@ -37,7 +37,7 @@ SIGNATURES = {
     "ckv_quest_score": ([_P, _I, _P, _P, _I, _I, _I, _P, _P], _I),
     "ckv_selection_overlap": ([_I, _I, _I, _P, _P, _I, _P, _P, _I, _P, _P], _I),
     "ckv_centroid_channels": ([_P, _P, _P, _P], _I),
-    "ckv_append_kv": ([_P, _P, _I, _I, _I, _I, _P, _P, _P], _I),
+    "ckv_append_kv": ([_P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P], _I),
     "ckv_channel_prescore": ([_P, _P, _I, _P, _P, _I, _P, _P, _P], _I),
     "ckv_cluster_incremental_begin": ([_P, _P, _I, _I, _I, _P], _I),
     "ckv_cluster_incremental_commit": ([_P, _P], _I),
@@ -268,9 +268,16 @@ def selection_overlap(prev, idx, count, hits, max_len: int, stream=None):
                                        _stream(stream)), "ckv_selection_overlap")
 
 
-def append_kv(k_new, v_new, K, V, pos: int, stream=None):
-    """Row ``pos`` of every unit of K and V := k_new[u], v_new[u] (see ckv_append_kv).
-    k_new / v_new may live in pinned host memory the device maps."""
-    units, max_len = K.shape[0], K.shape[1]
-    _check(lib().ckv_append_kv(ptr(k_new), ptr(v_new), _dtype_code(K), units, max_len, pos, ptr(K), ptr(V),
-                               _stream(stream)), "ckv_append_kv")
+def append_kv(k_src, v_src, K, V, pos: int, n: int | None = None, stream=None):
+    """Rows [pos, pos + n) of every unit of K and V := rows [0, n) of k_src /
+    v_src (see ckv_append_kv).  k_src / v_src are [units, d] (one row, n = 1)
+    or [units, src_len, d] (a view with a unit stride is taken as src_len =
+    that stride / d); they may live in pinned host memory the device maps."""
+    units, max_len, d = K.shape
+    if k_src.dim() == 2:
+        src_len, n = 1, 1
+    else:
+        src_len = k_src.stride(0) // d
+        n = k_src.shape[1] if n is None else n
+    _check(lib().ckv_append_kv(ptr(k_src), ptr(v_src), src_len, _dtype_code(K), units, max_len, pos, n, ptr(K),
+                               ptr(V), _stream(stream)), "ckv_append_kv")

@@ -1,12 +1,14 @@
-// Appending a decode step's K/V to the caches (ClusterKV page, section
-// "Clustering in semantic space", clustering strategy during inference: every
-// generated token's key and value join the KV cache and stay pending, attended
-// in full, until the next block of m tokens is clustered).
+// Appending keys and values to the caches (ClusterKV page, section "Clustering
+// in semantic space", clustering strategy during inference: every generated
+// token's key and value join the KV cache and stay pending, attended in full,
+// until the next block of m tokens is clustered; the prompt's K/V are the
+// cache the prefill clustering reads).
 //
-// One warp per unit copies the unit's new K row and V row (d elements each,
-// 16 bytes per lane) into row `pos` of K and V.  The sources may be device
-// memory or pinned host memory that the device maps (then the rows cross the
-// host link inside this kernel, with no separate copy).
+// For every unit, rows [0, n) of the sources go to rows [pos, pos + n) of K
+// and V.  The copy runs on the SMs in 16-byte vectors, several in flight per
+// lane, so the sources may be device memory or pinned host memory that the
+// device maps: then the rows cross the host link inside this kernel, with no
+// separate copy (one row per unit for a decode step; a whole prompt at once).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -15,16 +17,42 @@
 namespace ckv {
 namespace {
 
-// 16-byte chunks per row: D * elem / 16 (16 for bf16, 32 for fp32)
-__global__ void __launch_bounds__(256) append_kv_kernel(const uint4* __restrict__ k_new,
-                                                        const uint4* __restrict__ v_new, int units, int chunks,
-                                                        size_t row_stride, size_t pos_off, uint4* __restrict__ K,
-                                                        uint4* __restrict__ V) {
-    const int u = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-    if (u >= units) return;
-    for (int c = lane; c < chunks; c += 32) {
-        K[(size_t)u * row_stride + pos_off + c] = k_new[(size_t)u * chunks + c];
-        V[(size_t)u * row_stride + pos_off + c] = v_new[(size_t)u * chunks + c];
+constexpr int APPEND_THREADS = 256;
+constexpr int APPEND_UNROLL = 4;  // 16-byte vectors in flight per lane and tensor
+
+// grid (row blocks, units): block b of unit u copies the chunks
+// [b * span, (b + 1) * span) of the unit's n rows (chunks = 16-byte pieces,
+// `cpr` per row).
+__global__ void __launch_bounds__(APPEND_THREADS) append_kv_kernel(const uint4* __restrict__ k_src,
+                                                                   const uint4* __restrict__ v_src, size_t src_stride,
+                                                                   size_t n_chunks, size_t span, size_t dst_stride,
+                                                                   size_t dst_off, uint4* __restrict__ K,
+                                                                   uint4* __restrict__ V) {
+    const int u = blockIdx.y;
+    const size_t c0 = (size_t)blockIdx.x * span;
+    const size_t c1 = c0 + span < n_chunks ? c0 + span : n_chunks;
+    const uint4* ks = k_src + (size_t)u * src_stride;
+    const uint4* vs = v_src + (size_t)u * src_stride;
+    uint4* kd = K + (size_t)u * dst_stride + dst_off;
+    uint4* vd = V + (size_t)u * dst_stride + dst_off;
+    for (size_t c = c0 + threadIdx.x; c < c1; c += (size_t)APPEND_THREADS * APPEND_UNROLL) {
+        uint4 kr[APPEND_UNROLL], vr[APPEND_UNROLL];
+#pragma unroll
+        for (int j = 0; j < APPEND_UNROLL; ++j) {
+            const size_t cj = c + (size_t)j * APPEND_THREADS;
+            if (cj < c1) {
+                kr[j] = ks[cj];
+                vr[j] = vs[cj];
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < APPEND_UNROLL; ++j) {
+            const size_t cj = c + (size_t)j * APPEND_THREADS;
+            if (cj < c1) {
+                kd[cj] = kr[j];
+                vd[cj] = vr[j];
+            }
+        }
     }
 }
 
@@ -35,17 +63,22 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 using namespace ckv;
 
-extern "C" ckv_status ckv_append_kv(const void* k_new, const void* v_new, int32_t kv_dtype, int32_t units,
-                                    int32_t max_len, int32_t pos, void* K, void* V, void* stream) {
-    if (!k_new || !v_new || !K || !V) return CKV_ERR_ARG;
+extern "C" ckv_status ckv_append_kv(const void* k_src, const void* v_src, int32_t src_len, int32_t kv_dtype,
+                                    int32_t units, int32_t max_len, int32_t pos, int32_t n, void* K, void* V,
+                                    void* stream) {
+    if (!k_src || !v_src || !K || !V) return CKV_ERR_ARG;
     if (kv_dtype != CKV_F32 && kv_dtype != CKV_BF16) return CKV_ERR_DTYPE;
-    if (units < 1 || max_len < 1 || pos < 0 || pos >= max_len) return CKV_ERR_ARG;
-    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(K) || !aligned16(V)) return CKV_ERR_ALIGN;
+    if (units < 1 || max_len < 1 || n < 1 || src_len < n || pos < 0 || pos > max_len - n) return CKV_ERR_ARG;
+    if (!aligned16(k_src) || !aligned16(v_src) || !aligned16(K) || !aligned16(V)) return CKV_ERR_ALIGN;
     const int elem = kv_dtype == CKV_BF16 ? 2 : 4;
-    const int chunks = D * elem / 16;
-    const size_t row_stride = (size_t)max_len * chunks;  // per unit, in 16-byte chunks
-    append_kv_kernel<<<ceil_div(units, 8), 256, 0, (cudaStream_t)stream>>>(
-        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), units, chunks, row_stride,
-        (size_t)pos * chunks, static_cast<uint4*>(K), static_cast<uint4*>(V));
+    const size_t cpr = (size_t)D * elem / 16;  // 16-byte chunks per row
+    const size_t n_chunks = (size_t)n * cpr;
+    // up to 256 KB of each tensor per CTA
+    const size_t span = (size_t)APPEND_THREADS * APPEND_UNROLL * 16;
+    const size_t blocks = (n_chunks + span - 1) / span;
+    if (blocks > 0x7fffffffu || units > 65535) return CKV_ERR_ARG;
+    append_kv_kernel<<<dim3((unsigned)blocks, units), APPEND_THREADS, 0, (cudaStream_t)stream>>>(
+        static_cast<const uint4*>(k_src), static_cast<const uint4*>(v_src), (size_t)src_len * cpr, n_chunks, span,
+        (size_t)max_len * cpr, (size_t)pos * cpr, static_cast<uint4*>(K), static_cast<uint4*>(V));
     return cudaGetLastError() == cudaSuccess ? CKV_OK : CKV_ERR_CUDA;
 }
