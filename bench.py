@@ -684,11 +684,23 @@ def run_e2e(ctx, w, K, V, Q, one_call=False, sync_incremental=False):
         for t in range(T):
             if zero_copy:
                 # the kernels read this step's q and new K/V rows from pinned host
-                # memory, and the attention writes its output there
-                ckv.append_kv(inp_h[t, nq:nq + nr].view(U, d), inp_h[t, nq + nr:].view(U, d), Kd, Vd, L + t,
-                              stream=s)
+                # memory, and the attention writes its output there.  The rows are
+                # read only by the attention: with separate calls they are appended
+                # on a side stream while the scoring and selection run
+                q, kh, vh = inp_h[t, :nq].view(U, g, d), inp_h[t, nq:nq + nr].view(U, d), inp_h[t, nq + nr:].view(U, d)
+                if one_call:
+                    ckv.append_kv(kh, vh, Kd, Vd, L + t, stream=s)
+                    incremental(t)
+                    decode(t, q, outh[t])
+                    continue
+                e_step[t].record(s)
+                sk.wait_event(e_step[t])
+                ckv.append_kv(kh, vh, Kd, Vd, L + t, stream=sk)
+                e_k[t].record(sk)
                 incremental(t)
-                decode(t, inp_h[t, :nq].view(U, g, d), outh[t])
+                ctx.select(q, B, idx, cnt)
+                s.wait_event(e_k[t])
+                ctx.sparse_decode_attn(q, Kd, Vd, idx, cnt, B, L + t + 1, outh[t])
                 continue
             # the step's three inputs in parallel: q, and the new K and V rows
             # straight into their place in the caches (one strided copy each)
