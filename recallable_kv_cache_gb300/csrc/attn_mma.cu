@@ -224,6 +224,9 @@ __global__ void __launch_bounds__(MW * 32, 1) attn_mma_kernel(const MmaArgs a) {
     issue(0, t_begin, ids0);
     issue(1, t_begin + 1, ids1);  // tiles past t_end have no rows: empty groups
     issue(2, t_begin + 2, ids2);
+    // the first unit's query while the first tiles are in flight
+    cur_u = t_begin / a.tpu;
+    reset(cur_u);
 
     for (int i = 0, t = t_begin; t < t_end; ++i, ++t) {
         const int st = i % NST;
