@@ -336,6 +336,35 @@ __global__ void __launch_bounds__(G * D) attn_mma_combine_kernel(const float* __
     const int w0 = (u * tpu) / tpw, w1 = (u * tpu + tpu - 1) / tpw;
     const int ns = min(w1 - w0 + 1, CMB_MAX_SLOTS);
     const float* pu = part + (size_t)u * max_slots * PW;
+    if (ns <= 8) {
+        // the usual case: each thread loads its head's (max, sum) of every slot
+        // with its own accumulator entries in one round trip and merges them in
+        // registers (the same operations in the same order as below)
+        const int h = tid / D, c = tid % D;
+        float mv[8], lv[8], av[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+            if (t < ns) {
+                const float* sp = pu + (size_t)t * PW + h * (D + 2);
+                mv[t] = sp[D];
+                lv[t] = sp[D + 1];
+                av[t] = sp[c];
+            }
+        float M = -INFINITY;
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+            if (t < ns) M = fmaxf(M, mv[t]);
+        float l = 0.f, acc = 0.f;
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+            if (t < ns) {
+                const float f = (mv[t] == -INFINITY) ? 0.f : exp2f(mv[t] - M);
+                l += lv[t] * f;
+                acc += av[t] * f;
+            }
+        out[((size_t)u * G + h) * D + c] = l > 0.f ? acc / l : 0.f;
+        return;
+    }
     // every slot's (max, sum) pair at once; the serial part below reads smem only
     for (int e = tid; e < ns * G; e += G * D) {
         const float* ms = pu + (size_t)(e / G) * PW + (e % G) * (D + 2) + D;
