@@ -59,7 +59,9 @@ constexpr int SCORE_UNROLL = 4;  // centroid rows in flight per lane group
 template <typename T, int G>
 __global__ void __launch_bounds__(256) score_kernel(const T* __restrict__ q,
                                                    const T* __restrict__ mu, int cmax, int C,
-                                                   float* __restrict__ scores, int stride) {
+                                                   float* __restrict__ scores, int stride,
+                                                   const int32_t* __restrict__ pf_sizes,
+                                                   const int32_t* __restrict__ pf_offsets) {
     constexpr int CPL = Vec<T>::N;   // channels per lane
     constexpr int LPR = D / CPL;     // lanes per centroid row
     constexpr int RPI = 32 / LPR;    // rows per warp-wide load
@@ -69,6 +71,14 @@ __global__ void __launch_bounds__(256) score_kernel(const T* __restrict__ q,
     const int sub = lane / LPR, li = lane % LPR;
     ptx::grid_dependency_wait();  // q may come from the previous kernel
     ptx::allow_dependent_launch();
+    // the selection that follows reads this unit's sizes and offsets first:
+    // one warp of the unit's first block pulls those rows into L2 meanwhile
+    if (pf_sizes && blockIdx.x == 0 && warp == 7) {
+        for (int b = lane * 32; b < C + 1; b += 32 * 32) {
+            if (b < C) ptx::prefetch_l2(pf_sizes + (size_t)u * cmax + b);
+            ptx::prefetch_l2(pf_offsets + (size_t)u * (cmax + 1) + b);
+        }
+    }
 
     float qs[CPL];
 #pragma unroll
@@ -958,12 +968,13 @@ cudaError_t launch_attn_t(const void* q, const void* K, const void* V, const int
 
 template <typename T>
 cudaError_t launch_score_t(const void* q, const void* mu, int g, int units, int cmax, int C,
-                           float* scores, int stride, cudaStream_t s) {
+                           float* scores, int stride, const int32_t* pf_sizes, const int32_t* pf_offsets,
+                           cudaStream_t s) {
     constexpr int RPW = (32 / (D / Vec<T>::N)) * SCORE_UNROLL;  // rows per warp
     dim3 grid((C + 8 * RPW - 1) / (8 * RPW), units);
 #define CKV_SCORE(G)                                                                                     \
     return launch_dependent(score_kernel<T, G>, grid, dim3(256), 0, s, (const T*)q, (const T*)mu, cmax, C, \
-                            scores, stride)
+                            scores, stride, pf_sizes, pf_offsets)
     switch (g) {
         case 1: CKV_SCORE(1);
         case 2: CKV_SCORE(2);
@@ -989,13 +1000,15 @@ cudaError_t launch_sel_t(const ckv_ctx* ctx, const float* scores, int stride, in
 }  // namespace
 
 cudaError_t launch_score(const ckv_ctx* ctx, const void* q, int C, float* scores, int stride,
-                         cudaStream_t s) {
+                         cudaStream_t s, bool prefetch_csr) {
     if (C <= 0) return cudaSuccess;
+    const int32_t* ps = prefetch_csr ? ctx->sizes : nullptr;
+    const int32_t* po = prefetch_csr ? ctx->offsets : nullptr;
     if (ctx->cfg.kv_dtype == CKV_BF16)
         return launch_score_t<__nv_bfloat16>(q, ctx->mu_s, ctx->cfg.g, ctx->cfg.units, ctx->cmax, C,
-                                             scores, stride, s);
+                                             scores, stride, ps, po, s);
     return launch_score_t<float>(q, ctx->mu_s, ctx->cfg.g, ctx->cfg.units, ctx->cmax, C, scores,
-                                 stride, s);
+                                 stride, ps, po, s);
 }
 
 cudaError_t launch_select(const ckv_ctx* ctx, const void* q, const float* scores, int stride, int C, int B,
@@ -1003,7 +1016,7 @@ cudaError_t launch_select(const ckv_ctx* ctx, const void* q, const float* scores
     if (!scores) {
         // scores of every cluster into the context's scratch (a many-CTA
         // stream over the centroid table), then the selection reads them
-        cudaError_t e = launch_score(ctx, q, C, ctx->scores, ctx->cmax, s);
+        cudaError_t e = launch_score(ctx, q, C, ctx->scores, ctx->cmax, s, true);
         if (e != cudaSuccess) return e;
         scores = ctx->scores;
         stride = ctx->cmax;

@@ -97,7 +97,7 @@ cudaError_t launch_incremental(const ckv_ctx* ctx, const void* K, int start, int
                                int C_old, int csr_base, cudaStream_t s);
 // scores[u][c] = sum_h q_h . mu_c, written with row stride `stride`
 cudaError_t launch_score(const ckv_ctx* ctx, const void* q, int C, float* scores, int stride,
-                         cudaStream_t s);
+                         cudaStream_t s, bool prefetch_csr = false);
 // selection for every unit: scores from q and the centroids (scores == null)
 // or from caller-given scores [units][stride]
 cudaError_t launch_select(const ckv_ctx* ctx, const void* q, const float* scores, int stride, int C, int B,
