@@ -191,18 +191,10 @@ __global__ void __launch_bounds__(1024, 1) sel_kernel(
         const int c = e * NT + tid;
         sk[c] = c < C ? rank_key(scr[e], c) : ~0ull;
     }
-    __shared__ int32_t wtot[32];  // per-warp sums of the sizes
-    {
-        int t = 0;
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-            szc[e * NT + tid] = szr[e];
-            offc[e * NT + tid] = ofr[e];
-            t += szr[e];
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(FULL, t, o);
-        if (lane == 0) wtot[warp] = t;
+    for (int e = 0; e < E; ++e) {
+        szc[e * NT + tid] = szr[e];
+        offc[e * NT + tid] = ofr[e];
     }
     __syncthreads();
 
@@ -222,7 +214,8 @@ __global__ void __launch_bounds__(1024, 1) sel_kernel(
     }
     __syncthreads();
     if (warp == 0) {
-        int tot = lane < nwarps ? wtot[lane] : 0;  // clustered tokens: the sum of all sizes
+        int tot = 0;  // clustered tokens: the sum of all sizes
+        for (int c = lane; c < C; c += 32) tot += szc[c];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(FULL, tot, o);
         uint64_t ch[4];
