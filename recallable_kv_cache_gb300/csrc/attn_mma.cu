@@ -17,10 +17,10 @@
 // keep about 16 significant bits.
 //
 // Work split: the attended set of each unit is cut into tiles of 16 rows;
-// every warp owns a contiguous range of tiles (persistent grid, one CTA of 8
-// warps per SM).  Each warp runs its own 3-stage shared-memory ring: 16-byte
+// every warp owns a contiguous range of tiles (persistent grid, one CTA of 12
+// warps per SM).  Each warp runs its own 2-stage shared-memory ring: 16-byte
 // cp.async copies (one commit group per tile) fill a stage while the warp
-// computes an earlier one, token ids are resolved four tiles ahead, and rows
+// computes an earlier one, token ids are resolved NST + 1 tiles ahead, and rows
 // sit at a 272-byte pitch so that ldmatrix is free of bank conflicts.  The warp keeps an online softmax (max, sum,
 // O^T) per unit and writes one partial per (unit, warp) when it leaves a
 // unit.  attn_mma_combine_kernel merges the partials of each unit in warp
@@ -36,7 +36,7 @@ namespace ckv {
 namespace {
 
 constexpr unsigned FULL = 0xffffffffu;
-constexpr int MW = 8;   // warps per CTA
+constexpr int MW = 12;  // warps per CTA
 constexpr int TR = 16;  // rows per tile
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
@@ -89,7 +89,7 @@ struct MmaArgs {
     int32_t* dev_err;
 };
 
-constexpr int NST = 3;                       // ring stages per warp
+constexpr int NST = 2;                       // ring stages per warp
 constexpr int PITCH = D * 2 + 16;             // 272-byte row pitch: conflict-free ldmatrix
 constexpr int TILE_BYTES = TR * PITCH;        // one 16-row K (or V) tile
 constexpr int STAGE_BYTES = 2 * TILE_BYTES;   // K then V
@@ -218,22 +218,24 @@ __global__ void __launch_bounds__(MW * 32, 1) attn_mma_kernel(const MmaArgs a) {
     };
 
     // ---- prologue: the first NST tiles in flight, ids of the next one ready
-    int ids0 = ids_for(t_begin), ids1 = ids_for(t_begin + 1), ids2 = ids_for(t_begin + 2);
-    int ids_pend = ids_for(t_begin + 3);
-    unsigned vb0 = valid_bits(ids0), vb1 = valid_bits(ids1), vb2 = valid_bits(ids2);
-    issue(0, t_begin, ids0);
-    issue(1, t_begin + 1, ids1);  // tiles past t_end have no rows: empty groups
-    issue(2, t_begin + 2, ids2);
+    unsigned vb[NST];  // valid-row bits of the tiles in the ring, oldest first
+#pragma unroll
+    for (int j = 0; j < NST; ++j) {
+        const int ids = ids_for(t_begin + j);
+        vb[j] = valid_bits(ids);
+        issue(j, t_begin + j, ids);  // tiles past t_end have no rows: empty groups
+    }
+    int ids_pend = ids_for(t_begin + NST);
     // the first unit's query while the first tiles are in flight
     cur_u = t_begin / a.tpu;
     reset(cur_u);
 
     for (int i = 0, t = t_begin; t < t_end; ++i, ++t) {
         const int st = i % NST;
-        const int ids_next = ids_for(t + 4);  // in flight during this tile
+        const int ids_next = ids_for(t + NST + 1);  // in flight during this tile
         ptx::cp_async_wait_group<NST - 1>();  // this lane's copies of tile t have landed
         __syncwarp();                          // ... and every other lane's
-        const unsigned valid = vb0;
+        const unsigned valid = vb[0];
         const int u = t / a.tpu;
         if (u != cur_u) {
             if (cur_u >= 0) flush(cur_u);
@@ -307,9 +309,9 @@ __global__ void __launch_bounds__(MW * 32, 1) attn_mma_kernel(const MmaArgs a) {
         __syncwarp();
         // the stage is free again: tile t + NST into it (an empty group past the end)
         issue(st, t + NST, ids_pend);
-        vb0 = vb1;
-        vb1 = vb2;
-        vb2 = valid_bits(ids_pend);
+#pragma unroll
+        for (int j = 0; j + 1 < NST; ++j) vb[j] = vb[j + 1];
+        vb[NST - 1] = valid_bits(ids_pend);
         ids_pend = ids_next;
     }
     ptx::cp_async_wait_all();
@@ -324,6 +326,7 @@ __global__ void __launch_bounds__(MW * 32, 1) attn_mma_kernel(const MmaArgs a) {
 // computed once into shared memory; the accumulator loads of all slots are
 // independent, so they are in flight together.
 constexpr int CMB_MAX_SLOTS = 256;
+constexpr int CMB_REG_SLOTS = 12;  // units with at most this many partials merge in registers
 
 template <int G>
 __global__ void __launch_bounds__(G * D) attn_mma_combine_kernel(const float* __restrict__ part, int tpu, int tpw,
@@ -336,14 +339,14 @@ __global__ void __launch_bounds__(G * D) attn_mma_combine_kernel(const float* __
     const int w0 = (u * tpu) / tpw, w1 = (u * tpu + tpu - 1) / tpw;
     const int ns = min(w1 - w0 + 1, CMB_MAX_SLOTS);
     const float* pu = part + (size_t)u * max_slots * PW;
-    if (ns <= 8) {
+    if (ns <= CMB_REG_SLOTS) {
         // the usual case: each thread loads its head's (max, sum) of every slot
         // with its own accumulator entries in one round trip and merges them in
         // registers (the same operations in the same order as below)
         const int h = tid / D, c = tid % D;
-        float mv[8], lv[8], av[8];
+        float mv[CMB_REG_SLOTS], lv[CMB_REG_SLOTS], av[CMB_REG_SLOTS];
 #pragma unroll
-        for (int t = 0; t < 8; ++t)
+        for (int t = 0; t < CMB_REG_SLOTS; ++t)
             if (t < ns) {
                 const float* sp = pu + (size_t)t * PW + h * (D + 2);
                 mv[t] = sp[D];
@@ -352,11 +355,11 @@ __global__ void __launch_bounds__(G * D) attn_mma_combine_kernel(const float* __
             }
         float M = -INFINITY;
 #pragma unroll
-        for (int t = 0; t < 8; ++t)
+        for (int t = 0; t < CMB_REG_SLOTS; ++t)
             if (t < ns) M = fmaxf(M, mv[t]);
         float l = 0.f, acc = 0.f;
 #pragma unroll
-        for (int t = 0; t < 8; ++t)
+        for (int t = 0; t < CMB_REG_SLOTS; ++t)
             if (t < ns) {
                 const float f = (mv[t] == -INFINITY) ? 0.f : exp2f(mv[t] - M);
                 l += lv[t] * f;
