@@ -37,15 +37,15 @@ METRIC = "sparse-decode tokens/s at 32k ctx, B=1024; K-means ms/layer; % of HBM 
 
 # DRAM bytes (read + write) of one attn_mma_kernel launch per algorithmic byte,
 # from one ncu capture of the current kernel on this workload (decode step 41:
-# 146.5 MB of DRAM traffic for 143.5 MB of algorithmic bytes).  The traffic of a
+# 146.3 MB of DRAM traffic for 143.5 MB of algorithmic bytes).  The traffic of a
 # launch is this ratio times its algorithmic bytes (both grow with the attended
 # rows).  Set to None whenever the kernel changes until it is captured again.
-ATTN_TRAFFIC_PER_ALG_BYTE = 146.517 / 143.525
+ATTN_TRAFFIC_PER_ALG_BYTE = 146.323 / 143.525
 # Same for the whole decode step (--path step); None: not captured as one unit.
 STEP_TRAFFIC_PER_ALG_BYTE = None
 STEP_TRAFFIC_SOURCE = "not captured for the whole step"
 ATTN_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch (decode step 41, "
-                       "146.5 MB for 143.5 MB algorithmic), scaled to the mean launch by algorithmic bytes")
+                       "146.3 MB for 143.5 MB algorithmic), scaled to the mean launch by algorithmic bytes")
 WORKLOAD = "decode_32k"
 
 
