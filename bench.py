@@ -222,10 +222,10 @@ def max_over_ranks(values, world: int, device="cuda"):
     return t.tolist()
 
 
-def job_value(world: int, decode_steps: int, step_ms: float) -> float:
-    """Whole-job throughput: decode tokens of all ranks / job time (the max
-    over ranks)."""
-    return world * decode_steps / (step_ms / 1000.0)
+def job_value(world: int, decode_steps: int, step_ms: float, batch: int = 1) -> float:
+    """Whole-job throughput: decode tokens of all ranks (every step decodes one
+    token for each of the `batch` sequences) / job time (the max over ranks)."""
+    return world * batch * decode_steps / (step_ms / 1000.0)
 
 
 def run_ours(args, w, rank, world, device):
@@ -743,7 +743,7 @@ def run_e2e(ctx, w, K, V, Q, one_call=False, sync_incremental=False):
               "decode_ms": ev[2].elapsed_time(ev[3])}
     h2d = 2 * U * L * d * 2 + T * (nq + 2 * nr) * 2
     d2h = T * U * g * d * 4
-    return {"value": T / dt, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+    return {"value": w.batch * T / dt, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "job_s": dt, "phases_ms": {k: round(v, 3) for k, v in phases.items()},
             "how": "public API calls recorded once into a CUDA graph and replayed; the prompt K/V, every "
                    "step's q and new K/V rows come from pinned host memory and every step's output goes "
@@ -795,7 +795,7 @@ def oracle_sample(w, budget_s, device_tensors=None):
     pre = statistics.mean(t[0] for t in times)
     dec = statistics.mean(t[1] for t in times)
     job_s = (pre + dec) * w.units
-    return {"tokens_per_s": w.decode_steps / job_s, "prefill_s_per_unit": pre, "decode_s_per_unit": dec,
+    return {"tokens_per_s": w.batch * w.decode_steps / job_s, "prefill_s_per_unit": pre, "decode_s_per_unit": dec,
             "units": len(times), "job_s": job_s}
 
 
@@ -826,8 +826,10 @@ def main():
            "path": "ckv_decode_step" if args.path == "step" else "ckv_select + ckv_sparse_decode_attn",
            "incremental": "inline before the step" if args.sync_incremental else
                           "side stream: begun at the step, overlapping it; committed before the next step",
-           "l2": "inputs larger than L2: 4.4 GB of K/V and 268 MB of queries resident; every decode "
-                 "step gathers ~166 MB of scattered rows (L2 is 129 MB); no flush"}
+           "l2": (f"inputs larger than L2: {2 * w.units * w.max_len * w.d * 2 / 1e9:.1f} GB of K/V and "
+                  f"{w.decode_steps * w.units * w.g * w.d * 2 / 1e6:.0f} MB of queries resident; a decode step "
+                  f"gathers ~{decode_bytes(w, w.decode_steps // 2, w.C, True)[0] / 1e6:.0f} MB of scattered rows "
+                  f"(L2 is 129 MB); no flush")}
 
     if args.impl == "reference":
         if rank != 0:
@@ -862,7 +864,7 @@ def main():
     step_ms, prefill_ms, decode_ms = r["step_ms"], r["prefill_ms"], r["decode_ms"]
     step_ms, prefill_ms, decode_ms = max_over_ranks([step_ms, prefill_ms, decode_ms], world)
     T = w.decode_steps
-    value = job_value(world, T, step_ms)
+    value = job_value(world, T, step_ms, w.batch)
     if r["one_call"]:
         # one ckv_decode_step call per step: its launch window covers the whole
         # step; its bytes are those of the whole step
@@ -897,7 +899,7 @@ def main():
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
-        "decode_tokens_per_s": world * T / (decode_ms / 1000.0),
+        "decode_tokens_per_s": world * w.batch * T / (decode_ms / 1000.0),
         "kmeans_ms_per_layer": prefill_ms * w.kv_heads / w.units,
         "decode_step_us": 1000.0 * decode_ms / T,
         "decode_roofline": {"bound": "hbm", "achieved": decode_gbs, "peak": hbm, "unit": "GB/s",

@@ -192,7 +192,8 @@ ckv_status ckv_score(ckv_ctx* ctx, const void* q, int32_t q_dtype, float* scores
  * in rank order, ascending inside a cluster (the trimmed cluster keeps its
  * lowest ids); count[u] = min(B, clustered tokens).  Entries past count are
  * left unchanged.  Errors: CKV_ERR_STATE (no clusters), CKV_ERR_ARG (B < 0),
- * CKV_ERR_CAPACITY (B > max_budget). */
+ * CKV_ERR_CAPACITY (B > max_budget), CKV_ERR_UNIMPLEMENTED (more than 8192
+ * clusters per unit: the ranking keeps one CTA's shared memory). */
 ckv_status ckv_select_scored(ckv_ctx* ctx, const float* scores, int32_t B, int32_t* idx,
                              int32_t* count, void* stream);
 

@@ -1026,6 +1026,7 @@ cudaError_t launch_select(const ckv_ctx* ctx, const void* q, const float* scores
     if (N <= 1024) return launch_sel_t<1>(ctx, scores, stride, C, N, B, idx, count, s);
     if (N == 2048) return launch_sel_t<2>(ctx, scores, stride, C, N, B, idx, count, s);
     if (N == 4096) return launch_sel_t<4>(ctx, scores, stride, C, N, B, idx, count, s);
+    if (N == 8192) return launch_sel_t<8>(ctx, scores, stride, C, N, B, idx, count, s);
     return cudaErrorInvalidValue;
 }
 

@@ -102,7 +102,7 @@ cudaError_t launch_score(const ckv_ctx* ctx, const void* q, int C, float* scores
 // or from caller-given scores [units][stride]
 cudaError_t launch_select(const ckv_ctx* ctx, const void* q, const float* scores, int stride, int C, int B,
                           int32_t* idx, int32_t* count, cudaStream_t s);
-constexpr int MAX_SELECT_CLUSTERS = 4096;
+constexpr int MAX_SELECT_CLUSTERS = 8192;
 // split-K sparse decode attention; partials/counters are caller-provided scratch
 // (the counters serve the fp32 kernel's in-kernel combine only)
 cudaError_t launch_attention(const void* q, const void* K, const void* V, const int32_t* idx,

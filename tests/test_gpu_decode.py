@@ -181,7 +181,7 @@ def test_select_ties_and_empty_clusters():
     ctx.close()
 
 
-@pytest.mark.parametrize("C", [129, 1500, 3000])
+@pytest.mark.parametrize("C", [129, 1500, 3000, 6000])
 def test_select_large_cluster_counts(C):
     """Random CSR with many clusters (the sort then holds 1, 2 or 4 keys per
     thread), tied scores, empty clusters: selection from given scores against
