@@ -63,7 +63,7 @@ typedef enum {
     CKV_ERR_CUDA = -4,          /* a CUDA runtime call failed */
     CKV_ERR_TIMEOUT = -5,       /* a bounded device wait gave up */
     CKV_ERR_DEVICE_CHECK = -6,  /* a device-side check failed (see ckv_get_device_error) */
-    CKV_ERR_UNIMPLEMENTED = -7, /* configuration not supported by this build */
+    CKV_ERR_UNIMPLEMENTED = -7, /* configuration the library does not support */
     CKV_ERR_ALIGN = -8,         /* pointer not 16-byte aligned */
     CKV_ERR_STATE = -9          /* call out of order (e.g. select before clustering) */
 } ckv_status;

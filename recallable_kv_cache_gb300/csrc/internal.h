@@ -7,7 +7,7 @@
 
 namespace ckv {
 
-constexpr int D = 128;             // head dimension this build supports
+constexpr int D = 128;             // head dimension the kernels support
 constexpr int CSR_CHUNK = 1024;    // tokens per block in the CSR count/scatter passes
 constexpr int SEG_ROWS = 64;       // rows per centroid-update task
 constexpr int ASSIGN_TILE = 128;   // tokens per tcgen05 assignment tile (MMA M)
