@@ -7,7 +7,20 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+# Per-test wall-clock limit (seconds).  With the pytest-timeout plugin present
+# every test gets it (unless it sets its own); the thread method ends the whole
+# process, so a test stuck inside a CUDA call cannot keep the GPU busy.
+TEST_TIMEOUT_S = 900
+
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
     config.addinivalue_line("markers", "slow: long-running CPU test")
+
+
+def pytest_collection_modifyitems(config, items):
+    if not config.pluginmanager.hasplugin("timeout"):
+        return
+    for item in items:
+        if item.get_closest_marker("timeout") is None:
+            item.add_marker(pytest.mark.timeout(TEST_TIMEOUT_S, method="thread"))

@@ -148,55 +148,75 @@ def test_update_empty_cluster_keeps_centroid():
     ctx.close()
 
 
-def _free_running(w, iters, units):
-    """Run the GPU prefill and the oracle K-means on the same keys.  When the
-    oracle's trajectory has no near-tie row in any iteration, the GPU must
-    reproduce it exactly (labels, CSR) with centroids within 1e-5."""
+def labels_from_csr(sizes, offsets, perm, first_token, n):
+    """The label of every token of a cluster segment [first_token, first_token
+    + n), recovered from its CSR (and the CSR's invariants checked)."""
+    C = len(sizes)
+    assert sizes.sum() == n
+    assert np.array_equal(offsets[1:] - offsets[:-1], sizes)
+    assert np.array_equal(np.sort(perm), np.arange(first_token, first_token + n))
+    lab = np.empty(n, dtype=np.int64)
+    for c in range(C):
+        seg = perm[offsets[c] - offsets[0]:offsets[c + 1] - offsets[0]]
+        assert np.all(np.diff(seg) > 0)
+        lab[seg - first_token] = c
+    return lab
+
+
+def _lockstep_chain(w, iters, units):
+    """The GPU prefill run for k = 1 .. iters Lloyd iterations (it is
+    deterministic, so the run of k iterations passes through the states of
+    the run of k - 1).  Every iteration k of every unit is checked against
+    the oracle's step applied to the GPU's own state after k - 1 iterations:
+    the labels (recovered from the CSR) by the assignment rule, the CSR
+    bit-exact given those labels, the centroids within 1e-5 of the means.
+    Iteration 1 starts from the seeds, which both sides take from the keys.
+    While the GPU labels equal those of the oracle's own free-running
+    trajectory, the centroids must also agree with that trajectory; returns
+    the number of (unit, iteration) pairs on it and the near-tie rows seen."""
     K, _ = synth.make_kv(w)
-    ctx = make_ctx(units, w.g, w.max_len, w.C, 64, w.dtype, iters=iters)
-    ctx.cluster_prefill(K.cuda().contiguous(), w.L, w.C)
-    st = export_state(ctx, units, dtype=w.dtype)
-    ctx.close()
-    exact_units = 0
-    for u in range(units):
-        keys = to64(K[u, 16:w.L])
-        r = ck.cluster_prefill(to64(K[u]), w.L, w.C, iters=iters, operand=operand(w), trace=True)
-        near = 0
-        for stp in r["trace"]:
-            mu32 = stp["mu_in"].astype(np.float32).astype(np.float64)
-            lab = ck.assign(keys, ck.normalize_centroids(mu32, operand(w))[0])
-            _, nr = check_assignment(keys, mu32, lab, operand(w))
-            near += nr
-        # invariants that hold whatever the trajectory
-        assert st["sizes"][u].sum() == w.L - 16
-        assert np.array_equal(np.sort(st["perm"][u]), np.arange(16, w.L))
-        lab_gpu = np.empty(w.L - 16, dtype=np.int64)
-        for c in range(w.C):
-            seg = st["perm"][u][st["offsets"][u][c]:st["offsets"][u][c + 1]]
-            assert np.all(np.diff(seg) > 0)
-            lab_gpu[seg - 16] = c
-        if near == 0:
-            assert np.array_equal(st["sizes"][u], r["sizes"])
-            assert np.array_equal(st["offsets"][u], r["offsets"])
-            assert np.array_equal(st["perm"][u], r["perm"])
-            check_centroids(st["mu"][u], r["mu"])
-            exact_units += 1
-        # the GPU centroids are the means of the GPU clusters
-        check_centroids(st["mu"][u][st["sizes"][u] > 0],
-                        ck.update(keys, lab_gpu, st["mu"][u])[st["sizes"][u] > 0])
-    return exact_units
+    Kd = K.cuda().contiguous()
+    op = operand(w)
+    n = w.L - 16
+    keys = [to64(K[u, 16:w.L]) for u in range(units)]
+    prev = [ck.seed_centroids(keys[u], w.C).astype(np.float32).astype(np.float64) for u in range(units)]
+    traj = [ck.kmeans(keys[u], w.C, iters, op, trace=True)["trace"] for u in range(units)]
+    on_traj = [True] * units
+    exact, near_rows = 0, 0
+    for k in range(1, iters + 1):
+        ctx = make_ctx(units, w.g, w.max_len, w.C, 64, w.dtype, iters=k)
+        ctx.cluster_prefill(Kd, w.L, w.C)
+        st = export_state(ctx, units, dtype=w.dtype)
+        ctx.close()
+        for u in range(units):
+            lab = labels_from_csr(st["sizes"][u], st["offsets"][u], st["perm"][u], 16, n)
+            _, near = check_assignment(keys[u], prev[u], lab, op)
+            near_rows += near
+            sizes, offs, perm = ck.build_csr(lab, w.C, 16)
+            assert np.array_equal(st["sizes"][u], sizes) and np.array_equal(st["offsets"][u], offs)
+            assert np.array_equal(st["perm"][u], perm)
+            check_centroids(st["mu"][u], ck.update(keys[u], lab, prev[u]))
+            if on_traj[u] and np.array_equal(lab, traj[u][k - 1]["labels"]):
+                check_centroids(st["mu"][u], traj[u][k - 1]["mu_out"])
+                exact += 1
+            else:
+                on_traj[u] = False
+            prev[u] = st["mu"][u]
+    return exact, near_rows
 
 
 def test_prefill_tiny_fp32_full_config():
     """The tiny single-head workload at its full size: 2048 fp32 keys, C = 25,
     10 iterations, seeds at stride 80."""
     w = synth.WORKLOADS["tiny_2k"]
-    _free_running(w, 10, 1)
+    exact, _ = _lockstep_chain(w, 10, 1)
+    assert exact >= 1
 
 
 def test_prefill_bf16_free_running():
     w = workload("layer_32k", units=2, L=16 + 4000, decode_steps=0, C=50, n_centres=50)
-    _free_running(w, 10, 2)
+    exact, _ = _lockstep_chain(w, 10, 2)
+    assert exact >= 1
 
 
 def test_prefill_is_deterministic():
@@ -213,44 +233,58 @@ def test_prefill_is_deterministic():
         assert np.array_equal(outs[0][k], outs[1][k]), k
 
 
-@pytest.mark.parametrize("iters", [1, 10])
-def test_incremental(iters):
+def test_incremental():
     """Prefill, then two incremental clusterings of 320 tokens into 4
-    clusters each, appended after the prefill clusters."""
+    clusters each, appended after the prefill clusters; run for k = 1 .. 10
+    Lloyd iterations, every iteration of every block checked in lock step
+    against the oracle's step from the GPU's state after k - 1 iterations
+    (iteration 1 from the seeds, keys at stride 80 on both sides)."""
     w = workload("layer_32k", units=2, L=16 + 800, decode_steps=700, C=10, n_centres=10)
     K, _ = synth.make_kv(w)
     Kd = K.cuda().contiguous()
-    ctx = make_ctx(2, 4, w.max_len, 10 + 8, 64, "bf16", iters=iters)
-    ctx.cluster_prefill(Kd, w.L, 10)
-    base = export_state(ctx, 2)
-    ctx.cluster_incremental(Kd, w.L, 320, 4)
-    ctx.cluster_incremental(Kd, w.L + 320, 320, 4)
-    inf = ctx.info()
-    assert inf.n_clusters == 18 and inf.clustered_end == w.L + 640
-    st = export_state(ctx, 2)
-    ctx.close()
-    for u in range(2):
-        # prefill part unchanged
-        assert np.array_equal(st["sizes"][u][:10], base["sizes"][u])
-        assert np.array_equal(st["perm"][u][: w.L - 16], base["perm"][u])
-        for r in range(2):
+    blocks = [(u, r) for u in range(2) for r in range(2)]
+    keys = {b: to64(K[b[0], w.L + 320 * b[1]:w.L + 320 * (b[1] + 1)]) for b in blocks}
+    prev = {b: ck.seed_centroids(keys[b], 4).astype(np.float32).astype(np.float64) for b in blocks}
+    traj = {b: ck.kmeans(keys[b], 4, 10, "bf16", trace=True)["trace"] for b in blocks}
+    on_traj = {b: True for b in blocks}
+    exact = 0
+    base = None
+    for k in range(1, 11):
+        ctx = make_ctx(2, 4, w.max_len, 10 + 8, 64, "bf16", iters=k)
+        ctx.cluster_prefill(Kd, w.L, 10)
+        pre = export_state(ctx, 2)
+        ctx.cluster_incremental(Kd, w.L, 320, 4)
+        ctx.cluster_incremental(Kd, w.L + 320, 320, 4)
+        inf = ctx.info()
+        assert inf.n_clusters == 18 and inf.clustered_end == w.L + 640
+        st = export_state(ctx, 2)
+        assert ctx.device_error() == 0
+        ctx.close()
+        for u in range(2):
+            # the prefill part is unchanged by the appends
+            assert np.array_equal(st["sizes"][u][:10], pre["sizes"][u])
+            assert np.array_equal(st["perm"][u][:w.L - 16], pre["perm"][u])
+        for (u, r) in blocks:
+            b = (u, r)
             start = w.L + 320 * r
-            inc = ck.cluster_incremental(to64(K[u]), start, 320, 4, iters=iters, operand="bf16", trace=True)
-            keys = to64(K[u, start:start + 320])
-            near = sum(check_assignment(keys, s["mu_in"].astype(np.float32).astype(np.float64),
-                                        ck.assign(keys, ck.normalize_centroids(
-                                            s["mu_in"].astype(np.float32).astype(np.float64), "bf16")[0]),
-                                        "bf16")[1] for s in inc["trace"])
             cs = slice(10 + 4 * r, 14 + 4 * r)
             seg_lo = st["offsets"][u][10 + 4 * r]
             assert seg_lo == w.L - 16 + 320 * r
-            got_perm = st["perm"][u][seg_lo: seg_lo + 320]
-            assert np.array_equal(np.sort(got_perm), np.arange(start, start + 320))
-            if near == 0:
-                assert np.array_equal(st["sizes"][u][cs], inc["sizes"])
-                assert np.array_equal(st["offsets"][u][cs] - seg_lo, inc["offsets"][:4])
-                assert np.array_equal(got_perm, inc["perm"])
-                check_centroids(st["mu"][u][cs], inc["mu"])
+            sizes, offs = st["sizes"][u][cs], st["offsets"][u][10 + 4 * r:15 + 4 * r]
+            perm = st["perm"][u][seg_lo:seg_lo + 320]
+            lab = labels_from_csr(sizes, offs, perm, start, 320)
+            check_assignment(keys[b], prev[b], lab, "bf16")
+            wsz, woff, wperm = ck.build_csr(lab, 4, start)
+            assert np.array_equal(sizes, wsz) and np.array_equal(offs - seg_lo, woff)
+            assert np.array_equal(perm, wperm)
+            check_centroids(st["mu"][u][cs], ck.update(keys[b], lab, prev[b]))
+            if on_traj[b] and np.array_equal(lab, traj[b][k - 1]["labels"]):
+                check_centroids(st["mu"][u][cs], traj[b][k - 1]["mu_out"])
+                exact += 1
+            else:
+                on_traj[b] = False
+            prev[b] = st["mu"][u][cs]
+    assert exact >= 1
 
 
 def test_incremental_begin_commit():

@@ -257,12 +257,133 @@ def pin_append_clusters(m):
         assert np.array_equal(seg, want)
 
 
+def pin_attention_tokens_with_pending(m):
+    """The attended set while decode tokens are pending (section "Clustering
+    in semantic space", clustering strategy during inference: tokens are
+    clustered in blocks of m, so the newest ones are not yet in any cluster):
+    the sinks, every position in [clustered_end, cur_len) and the selected
+    tokens, listed here by hand.  Attention over that set is checked against
+    torch's scaled-dot-product attention over the same hand-listed rows."""
+    idx = np.array([50, 17, 99, 23])
+    got = m.attention_tokens(16, 100, 104, idx)
+    want = list(range(16)) + [100, 101, 102, 103] + [50, 17, 99, 23]
+    assert list(got) == want
+    # nothing pending: sinks and the selection only
+    assert list(m.attention_tokens(16, 100, 100, idx)) == list(range(16)) + [50, 17, 99, 23]
+    # one pending token (the usual decode step right after a clustering)
+    assert list(m.attention_tokens(4, 9, 10, np.array([5]))) == [0, 1, 2, 3, 9, 5]
+    # no selection (budget 0): sinks and pending only
+    assert list(m.attention_tokens(2, 7, 9, np.array([], dtype=np.int64))) == [0, 1, 7, 8]
+    rng = np.random.default_rng(13)
+    K = rng.standard_normal((110, 128))
+    V = rng.standard_normal((110, 128))
+    q = rng.standard_normal((4, 128))
+    rows = want
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q)[None], torch.from_numpy(K[rows])[None], torch.from_numpy(V[rows])[None])[0].numpy()
+    out = m.sparse_attention(q, K, V, m.attention_tokens(16, 100, 104, idx))
+    assert np.abs(out - ref).max() < 1e-12
+
+
+def _f32_normalisations(mu):
+    """Float32 normalisations of the rows of mu the way a GPU may compute
+    them: the sum of squares as 32 lanes of 4 sequential terms followed by a
+    butterfly over the lanes, or numpy's pairwise float32 sum; then sqrt and a
+    division, or a multiplication by the reciprocal (all float32)."""
+    m32 = np.asarray(mu, dtype=np.float32)
+    sq = m32 * m32
+    lanes = sq.reshape(len(m32), 32, -1)
+    acc = lanes[:, :, 0].copy()
+    for j in range(1, lanes.shape[2]):
+        acc = (acc + lanes[:, :, j]).astype(np.float32)
+    w = 16
+    while w >= 1:
+        acc = (acc + np.roll(acc, -w, axis=1)).astype(np.float32)
+        w //= 2
+    tree = acc[:, 0]
+    pair = sq.sum(axis=1, dtype=np.float32)
+    outs = []
+    for ss in (tree, pair):
+        nrm = np.sqrt(ss.astype(np.float32)).astype(np.float32)[:, None]
+        outs.append((m32 / nrm).astype(np.float32))
+        outs.append((m32 * (np.float32(1.0) / nrm).astype(np.float32)).astype(np.float32))
+    return outs
+
+
+def pin_rounding_band(m):
+    """The ambiguity band of the bf16 centroid directions (used by the GPU
+    acceptance rule for arg-max decisions): wherever any float32
+    normalisation, or any relative perturbation of the exact unit vector up to
+    2^-20, rounds to another bfloat16 than the exact value, the band holds
+    that difference; the band is one bfloat16 step exactly where the exact
+    value lies within 2^-20 (relative) of a rounding midpoint, and 0
+    everywhere else."""
+    rng = np.random.default_rng(14)
+    mu = rng.standard_normal((64, 128)) * rng.uniform(0.01, 50.0, size=(64, 1))
+    mu[:, 5] *= 20.0
+    # rows with one component of the unit vector planted next to a bf16
+    # midpoint (relative offsets 2^-26 .. 2^-18 from a (k + 1/2) step, both
+    # sides): y_j = t sqrt(S / (1 - t^2)) gives y_j / ||y|| = t, S = the sum of
+    # the other squares
+    planted = []
+    for r in range(160):
+        y = rng.standard_normal(128)
+        j = int(rng.integers(0, 128))
+        y[j] = 0.0
+        S = float(y @ y)
+        t0 = rng.uniform(0.05, 0.9) * rng.choice([-1, 1])
+        mant, ex = np.frexp(t0)
+        t = float(np.ldexp(np.floor(mant * 256.0) + 0.5, ex - 8))
+        t *= 1.0 + rng.choice([-1, 1]) * 2.0 ** rng.uniform(-26, -18)
+        y[j] = t * math.sqrt(S / (1.0 - t * t))
+        planted.append(y * rng.uniform(0.5, 3.0))
+    mu = np.concatenate([mu, np.array(planted)])
+    rel = 2.0 ** -20
+    mh, amb = m.normalize_centroids(mu, "bf16", rel_err=rel)
+    xe = mu / np.linalg.norm(mu, axis=1, keepdims=True)
+    # 1. the band is 0 or exactly one bf16 step of the exact value
+    mant, ex = np.frexp(xe)
+    step = np.ldexp(np.ones_like(xe), ex - 8)
+    assert np.all((amb == 0) | np.isclose(amb, step, rtol=0, atol=0) | np.isclose(amb, step / 2, rtol=0, atol=0))
+    # 2. non-zero exactly where the exact value is within rel of a midpoint
+    #    (strictly inside, or strictly outside by a margin: skip the knife edge)
+    t = mant * 256.0
+    dist = np.abs(t - (np.floor(t) + 0.5)) / np.abs(t)   # relative distance to the midpoint
+    inside, outside = dist < rel * 0.999, dist > rel * 1.001
+    assert np.all(amb[inside] > 0) and np.all(amb[outside] == 0)
+    assert inside.sum() >= 50 and outside.sum() >= 1000
+    # 3. every float32 normalisation and every perturbation within rel rounds
+    #    to the exact rounding or to the other side of the band
+    for x32 in _f32_normalisations(mu):
+        got = m.round_to_bf16(x32.astype(np.float64))
+        assert np.all(np.abs(got - mh) <= amb), np.abs(got - mh)[np.abs(got - mh) > amb][:5]
+    for k in range(-16, 17):
+        got = m.round_to_bf16(xe * (1.0 + rel * k / 16.0))
+        assert np.all(np.abs(got - mh) <= amb)
+    # 4. far from midpoints, the band is empty (float64 operands: always empty)
+    assert not m.normalize_centroids(mu, "f64")[1].any()
+
+
+def pin_objective_hand_value(m):
+    """J = sum_i (1 - cos(k_i, mu_c(i))) on a hand-computed example: k = (1,0),
+    (0,1), (1,1), (0,0) with labels 0, 0, 1, 1 and centroids (3,0), (0,2):
+    cosines 1, 0, 1/sqrt(2) and 0 (a zero key), so J = 3 - 1/sqrt(2)."""
+    keys = np.array([[1.0, 0.0], [0.0, 1.0], [1.0, 1.0], [0.0, 0.0]])
+    labels = np.array([0, 0, 1, 1], dtype=np.int32)
+    mu = np.array([[3.0, 0.0], [0.0, 2.0]])
+    assert abs(m.objective(keys, labels, mu) - (3.0 - 1.0 / math.sqrt(2.0))) < 1e-15
+    # perfect clusters: J = 0; opposite centroid: D = 2
+    assert m.objective(keys[:1], labels[:1], mu) == 0.0
+    assert abs(m.objective(np.array([[-1.0, 0.0]]), np.array([0], dtype=np.int32), mu) - 2.0) < 1e-15
+
+
 PINS = [pin_selection_worked_example, pin_cluster_count, pin_bf16_rounding,
         pin_assign_vs_scipy_cosine, pin_assign_brute_force, pin_update_closed_form,
         pin_update_is_mean_logit, pin_planted_partition,
         pin_one_token_per_cluster_is_exact_top_b, pin_selection_vs_token_sort,
         pin_attention_vs_torch_sdpa, pin_assignment_never_increases_objective,
-        pin_recall_properties, pin_append_clusters]
+        pin_recall_properties, pin_append_clusters, pin_attention_tokens_with_pending,
+        pin_rounding_band, pin_objective_hand_value]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
@@ -355,9 +476,61 @@ def _mut_bf16_truncate(mod):
     mod.round_to_bf16 = round_to_bf16
 
 
+def _mut_pending_past_end(mod):
+    def attention_tokens(sinks, clustered_end, cur_len, idx):
+        return np.concatenate([np.arange(sinks), np.arange(clustered_end, cur_len + 1),
+                               np.asarray(idx, dtype=np.int64)]).astype(np.int64)
+    mod.attention_tokens = attention_tokens
+
+
+def _mut_pending_from_one_early(mod):
+    def attention_tokens(sinks, clustered_end, cur_len, idx):
+        return np.concatenate([np.arange(sinks), np.arange(clustered_end - 1, cur_len),
+                               np.asarray(idx, dtype=np.int64)]).astype(np.int64)
+    mod.attention_tokens = attention_tokens
+
+
+def _mut_pending_dropped(mod):
+    def attention_tokens(sinks, clustered_end, cur_len, idx):
+        return np.concatenate([np.arange(sinks), np.asarray(idx, dtype=np.int64)]).astype(np.int64)
+    mod.attention_tokens = attention_tokens
+
+
+def _mut_band_too_wide(mod):
+    orig = mod.normalize_centroids
+    mod.normalize_centroids = lambda mu, operand="bf16", rel_err=2.0 ** -20: orig(mu, operand, 2.0 ** -12)
+
+
+def _mut_band_missing(mod):
+    orig = mod.normalize_centroids
+    mod.normalize_centroids = lambda mu, operand="bf16", rel_err=2.0 ** -20: (
+        orig(mu, operand, rel_err)[0], np.zeros_like(np.asarray(mu, dtype=np.float64)))
+
+
+def _mut_band_two_steps(mod):
+    orig = mod.normalize_centroids
+    mod.normalize_centroids = lambda mu, operand="bf16", rel_err=2.0 ** -20: (
+        orig(mu, operand, rel_err)[0], 2.0 * orig(mu, operand, rel_err)[1])
+
+
+def _mut_objective_offset(mod):
+    orig = mod.objective
+    mod.objective = lambda keys, labels, mu: orig(keys, labels, mu) + 1.0
+
+
+def _mut_objective_plus_cos(mod):
+    def objective(keys, labels, mu):
+        mu_hat, _ = mod.normalize_centroids(mu, "f64")
+        cos = mod.cosine_to_centroids(keys, mu_hat)
+        return float(np.sum(1.0 + cos[np.arange(len(labels)), labels]))
+    mod.objective = objective
+
+
 MUTANTS = [_mut_argmin, _mut_sum_update, _mut_normalised_mean, _mut_no_trim,
            _mut_ascending_rank, _mut_no_scale, _mut_cosine_score, _mut_seed_stride_one,
-           _mut_transposed_dot, _mut_bf16_truncate]
+           _mut_transposed_dot, _mut_bf16_truncate, _mut_pending_past_end, _mut_pending_from_one_early,
+           _mut_pending_dropped, _mut_band_too_wide, _mut_band_missing, _mut_band_two_steps,
+           _mut_objective_offset, _mut_objective_plus_cos]
 
 
 @pytest.mark.parametrize("mutate", MUTANTS, ids=lambda f: f.__name__)
@@ -368,6 +541,6 @@ def test_mutant_caught(mutate):
     for pin in PINS:
         try:
             pin(mod)
-        except AssertionError:
+        except Exception:  # a failed check, or a crash on the planted mistake
             failed.append(pin.__name__)
     assert failed, f"no pin caught {mutate.__name__}"
