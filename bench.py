@@ -35,17 +35,12 @@ from recallable_kv_cache_gb300 import synth  # noqa: E402
 
 METRIC = "sparse-decode tokens/s at 32k ctx, B=1024; K-means ms/layer; % of HBM roofline"
 
-# DRAM bytes (read + write) of one attn_mma_kernel launch per algorithmic byte,
-# from one ncu capture of the current kernel on this workload (decode step 41:
-# 146.3 MB of DRAM traffic for 143.5 MB of algorithmic bytes).  The traffic of a
-# launch is this ratio times its algorithmic bytes (both grow with the attended
-# rows).  Set to None whenever the kernel changes until it is captured again.
-ATTN_TRAFFIC_PER_ALG_BYTE = 146.323 / 143.525
-# Same for the whole decode step (--path step); None: not captured as one unit.
+# DRAM bytes (read + write) of one decode step (the kernels of one
+# ckv_decode_step) per algorithmic byte, from one ncu capture of the current
+# kernels; the traffic of a step is this ratio times its algorithmic bytes.
+# None whenever a kernel changes until it is captured again.
 STEP_TRAFFIC_PER_ALG_BYTE = None
-STEP_TRAFFIC_SOURCE = "not captured for the whole step"
-ATTN_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch (decode step 41, "
-                       "146.3 MB for 143.5 MB algorithmic), scaled to the mean launch by algorithmic bytes")
+STEP_TRAFFIC_SOURCE = "not captured for the current kernels"
 WORKLOAD = "decode_32k"
 
 
@@ -58,7 +53,8 @@ def parse():
     p.add_argument("--workload", default=WORKLOAD)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget")
+    p.add_argument("--no-comparators", action="store_true", help="skip the Quest / reuse / channel / full-KV side "
+                                                                  "measurements")
     p.add_argument("--units", type=int, default=0, help="override the unit count (small profiling cases)")
     p.add_argument("--decode-steps", type=int, default=0, help="override the decode steps (profiling)")
     p.add_argument("--sync-incremental", action="store_true",
@@ -235,13 +231,16 @@ def run_ours(args, w, rank, world, device):
     U, L, B, T = w.units, w.L, w.B, w.decode_steps
     K, V = synth.make_kv(w, device="cuda")
     Q = synth.make_queries(w, T, device="cuda")
+    # the K/V row each decode step appends (rows L .. L + T - 1 of the cache,
+    # kept apart so that every step really copies its row into the cache)
+    Knew, Vnew = K[:, L:L + T].clone(), V[:, L:L + T].clone()
     torch.cuda.synchronize()
     ctx = ckv.Context(units=U, g=w.g, max_len=w.max_len, max_clusters=w.max_clusters, max_budget=B,
                       iters=w.iters, m=w.m, c_plus=w.c_plus)
     idx = torch.empty(U, B, dtype=torch.int32, device="cuda")
     cnt = torch.empty(U, dtype=torch.int32, device="cuda")
     out = torch.empty(U, w.g, w.d, dtype=torch.float32, device="cuda")
-    ext = ExternalEvents()
+    one_call = args.path == "step"
 
     # eager pass first (validates every call), then capture
     ctx.cluster_prefill(K, L, w.C)
@@ -249,54 +248,40 @@ def run_ours(args, w, rank, world, device):
     s = torch.cuda.Stream()
     side = torch.cuda.Stream()
     fork = torch.cuda.Event()
+
+    def decode_loop(sync_incremental):
+        """Every decode step of the job: append the step's K/V row, cluster the
+        last m tokens every m steps (on a side stream overlapping the step,
+        committed before the next one; or inline), then the decode step."""
+        commit_at = -1
+        for t in range(T):
+            ckv.append_kv(Knew[:, t:t + 1], Vnew[:, t:t + 1], K, V, L + t, stream=s)
+            if t > 0 and t % w.m == 0:
+                if sync_incremental:
+                    ctx.cluster_incremental(K, L + t - w.m, stream=s)
+                else:
+                    fork.record(s)
+                    side.wait_event(fork)
+                    ctx.cluster_incremental_begin(K, L + t - w.m, stream=side)
+                    commit_at = t + 1
+            if t == commit_at:
+                ctx.cluster_incremental_commit(stream=s)
+            if one_call:
+                ctx.decode_step(Q[t], K, V, B, L + t + 1, idx, cnt, out, stream=s)
+            else:
+                ctx.select(Q[t], B, idx, cnt, stream=s)
+                ctx.sparse_decode_attn(Q[t], K, V, idx, cnt, B, L + t + 1, out, stream=s)
+
     g_pre, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-    # per-kernel durations: event nodes around the ckv_decode_step calls (step
-    # path) or the select and attention launches (separate path) of every
-    # EVERY-th decode step (a uniform sample; events on every step would
-    # themselves slow the loop)
-    EVERY = 16
-    one_call = args.path == "step"
-    sampled = [t for t in range(T) if t % EVERY == 0]
-    ev = {t: [torch.cuda.Event(enable_timing=True) for _ in range(3)] for t in sampled}
-    for e3 in ev.values():  # torch creates the CUDA event on first record
-        for e in e3:
-            e.record(s)
-    s.synchronize()
-    # decode: score, select, attention, combine per step + one incremental kernel per block
-    launches = {"prefill": 1 + w.iters * 6, "decode": 4 * T + w.n_incremental}
+    # per step: append, score, select/step, attention + combine; plus one
+    # incremental kernel per block
+    per_step = 4 if one_call else 5
+    launches = {"prefill": 1 + w.iters * 6, "decode": per_step * T + w.n_incremental}
     with torch.cuda.stream(s):
         with torch.cuda.graph(g_pre, stream=s):
-            ctx.cluster_prefill(K, L, w.C)
+            ctx.cluster_prefill(K, L, w.C, stream=s)
         with torch.cuda.graph(g_dec, stream=s):
-            commit_at = -1
-            for t in range(T):
-                if t > 0 and t % w.m == 0:
-                    if args.sync_incremental:
-                        ctx.cluster_incremental(K, L + t - w.m)
-                    else:
-                        # fork a side stream: the clustering overlaps this step,
-                        # whose selection still sees the previous clusters
-                        fork.record(s)
-                        side.wait_event(fork)
-                        ctx.cluster_incremental_begin(K, L + t - w.m, stream=side)
-                        commit_at = t + 1
-                if t == commit_at:
-                    ctx.cluster_incremental_commit(stream=s)
-                q = Q[t]
-                if t in ev:
-                    ext.record(ev[t][0], s)
-                if one_call:
-                    ctx.decode_step(q, K, V, B, L + t + 1, idx, cnt, out)
-                    if t in ev:
-                        ext.record(ev[t][1], s)
-                        ext.record(ev[t][2], s)
-                else:
-                    ctx.select(q, B, idx, cnt)
-                    if t in ev:
-                        ext.record(ev[t][1], s)
-                    ctx.sparse_decode_attn(q, K, V, idx, cnt, B, L + t + 1, out)
-                    if t in ev:
-                        ext.record(ev[t][2], s)
+            decode_loop(args.sync_incremental)
     # clusters visible at step t (an asynchronous clustering begun at step t is
     # committed before step t + 1)
     C_at = [w.C + w.c_plus * ((t // w.m) if args.sync_incremental else max(0, (t - 1) // w.m)) for t in range(T)]
@@ -313,8 +298,6 @@ def run_ours(args, w, rank, world, device):
         if sample is not None:
             sample["prefill"].append(p0.elapsed_time(p1))
             sample["decode"].append(p1.elapsed_time(p2))
-            sample["select"].append(statistics.mean(ev[t][0].elapsed_time(ev[t][1]) for t in sampled))
-            sample["attn"].append(statistics.mean(ev[t][1].elapsed_time(ev[t][2]) for t in sampled))
 
     for _ in range(args.warmup):
         one_step(None)
@@ -327,7 +310,7 @@ def run_ours(args, w, rank, world, device):
     clk = ClockSampler(smi_index)
     clk.start()
     time.sleep(0.3)
-    sample = {"prefill": [], "decode": [], "select": [], "attn": []}
+    sample = {"prefill": [], "decode": []}
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
     for _ in range(args.steps):
@@ -343,27 +326,122 @@ def run_ours(args, w, rank, world, device):
 
     step_ms = [a + b for a, b in zip(sample["prefill"], sample["decode"])]
     res = dict(step_ms=sum(step_ms) / len(step_ms), prefill_ms=statistics.mean(sample["prefill"]),
-               decode_ms=statistics.mean(sample["decode"]), select_ms=statistics.mean(sample["select"]),
-               attn_ms=statistics.mean(sample["attn"]), wall_s=wall, clocks=clocks,
-               step_launch_ms=statistics.mean(a + b for a, b in zip(sample["select"], sample["attn"])),
+               decode_ms=statistics.mean(sample["decode"]), wall_s=wall, clocks=clocks,
                launches=(launches["prefill"] + launches["decode"]) * args.steps)
     ai = not args.sync_incremental
-    res["attn_bytes_per_launch"] = statistics.mean(decode_bytes(w, t, C_at[t], ai)[0] for t in sampled)
-    res["step_bytes_per_launch"] = statistics.mean(decode_bytes(w, t, C_at[t], ai)[1] for t in sampled)
     res["one_call"] = one_call
     res["decode_bytes_per_step"] = sum(decode_bytes(w, t, C_at[t], ai)[1] for t in range(T)) / T
+    res["step_timing"] = time_decode_steps(ctx, w, K, V, Q, Knew, Vnew, one_call)
+    if w.n_incremental > 0 and not args.sync_incremental:
+        res["async_clustering"] = hidden_clustering(ctx, w, K, g_pre, g_dec, decode_loop, s,
+                                                    statistics.mean(sample["decode"]))
     res["assign_ms"] = time_assign(ctx, w, K)
     res["recall"] = selection_recall(lambda q, i, c: ctx.select(q, w.B, i, c), w, K, Q)
-    res["reuse"] = selection_reuse(ctx, w)
-    res["quest"] = quest_comparator(w, K, V, Q)
-    res["channel_prescore"] = channel_prescore_comparator(w, K, Q)
-    res["full_kv"] = full_kv_attention(w, K, V, Q)
+    if not args.no_comparators:
+        res["reuse"] = selection_reuse(ctx, w)
+        res["quest"] = quest_comparator(w, K, V, Q)
+        res["channel_prescore"] = channel_prescore_comparator(w, K, Q)
+        res["full_kv"] = full_kv_attention(w, K, V, Q)
     res["w"] = w
     res["ctx"] = ctx
     res["tensors"] = (K, V, Q)
     if not args.no_e2e:
         res["e2e"] = run_e2e(ctx, w, K, V, Q, one_call, args.sync_incremental)
     return res
+
+
+def time_decode_steps(ctx, w, K, V, Q, Knew, Vnew, one_call, n=64, p_first=129, reps=5):
+    """The decode step timed on its own: `n` consecutive steps (append, then
+    the decode step) with p_first .. p_first + n - 1 pending tokens (around the
+    job's mean of ~160) over the prompt clusters, captured in one CUDA graph
+    with no event inside; CUDA events around `reps` whole replays give the
+    time per step.  For the per-kernel path the attention (+ combine) launch
+    is also timed alone the same way (a graph of n attention launches)."""
+    from recallable_kv_cache_gb300 import ckv
+    U, L, B = w.units, w.L, w.B
+    ctx.cluster_prefill(K, L, w.C)  # back to the prompt clusters
+    idx = torch.empty(U, B, dtype=torch.int32, device="cuda")
+    cnt = torch.empty(U, dtype=torch.int32, device="cuda")
+    out = torch.empty(U, w.g, w.d, dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    steps = [(p_first + i - 1, L + p_first + i) for i in range(n)]  # (row appended, cur_len)
+
+    def step(t, row, cur):
+        ckv.append_kv(Knew[:, row:row + 1], Vnew[:, row:row + 1], K, V, L + row, stream=s)
+        if one_call:
+            ctx.decode_step(Q[t], K, V, B, cur, idx, cnt, out, stream=s)
+        else:
+            ctx.select(Q[t], B, idx, cnt, stream=s)
+            ctx.sparse_decode_attn(Q[t], K, V, idx, cnt, B, cur, out, stream=s)
+
+    def timed(body):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            body()  # eager once: validates the calls
+            with torch.cuda.graph(g, stream=s):
+                body()
+            for _ in range(3):
+                g.replay()
+            e0.record(s)
+            for _ in range(reps):
+                g.replay()
+            e1.record(s)
+        torch.cuda.synchronize()
+        return 1000.0 * e0.elapsed_time(e1) / (reps * n)
+
+    step_us = timed(lambda: [step(i, row, cur) for i, (row, cur) in enumerate(steps)])
+    byts = statistics.mean(decode_bytes(w, row, w.C)[1] for row, _ in steps)
+    append_b = U * 2 * w.d * 2 * 2  # the new K and V rows: read and written
+    res = {"step_us": step_us, "bytes_per_step": byts + append_b, "pending": [steps[0][0] + 1, steps[-1][0] + 1],
+           "what": f"{n} decode steps (append + " + ("ckv_decode_step" if one_call else
+                                                        "ckv_select + ckv_sparse_decode_attn") +
+                   f") with {steps[0][0] + 1}..{steps[-1][0] + 1} pending tokens in one graph, "
+                   f"{reps} replays between two CUDA events"}
+    if not one_call:
+        ctx.select(Q[0], B, idx, cnt, stream=s)
+        cur = L + p_first + n // 2
+        res["attn_us"] = timed(lambda: [ctx.sparse_decode_attn(Q[i], K, V, idx, cnt, B, cur, out, stream=s)
+                                        for i in range(n)])
+        res["attn_bytes"] = decode_bytes(w, cur - L - 1, w.C)[0]
+    return res
+
+
+def hidden_clustering(ctx, w, K, g_pre, g_dec, decode_loop, s, async_ms, reps=2):
+    """How much of the incremental clustering the side stream hides: the same
+    decode loop with the clustering inline (a graph of its own), against the
+    asynchronous one, over the clustering kernel's own time (one incremental
+    clustering of every unit, timed alone): hidden = (inline - async) /
+    (blocks x clustering time)."""
+    torch.cuda.synchronize()
+    ctx.cluster_prefill(K, w.L, w.C)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        e0.record(s)
+        ctx.cluster_incremental(K, w.L, stream=s)
+        e1.record(s)
+    torch.cuda.synchronize()
+    incr_ms = e0.elapsed_time(e1)
+    ctx.cluster_prefill(K, w.L, w.C)
+    g_sync = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g_sync, stream=s):
+            decode_loop(True)
+        g_pre.replay()
+        g_sync.replay()
+        ts = []
+        for _ in range(reps):
+            g_pre.replay()
+            e0.record(s)
+            g_sync.replay()
+            e1.record(s)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+    sync_ms = statistics.mean(ts)
+    blocks = w.n_incremental
+    return {"decode_ms_async": async_ms, "decode_ms_inline": sync_ms, "incremental_ms": incr_ms,
+            "blocks": blocks, "hidden_fraction": (sync_ms - async_ms) / (blocks * incr_ms),
+            "what": "(inline - async decode loop) / (blocks x one incremental clustering timed alone)"}
 
 
 def time_assign(ctx, w, K, reps=5):
@@ -755,51 +833,45 @@ def run_e2e(ctx, w, K, V, Q, one_call=False, sync_incremental=False):
 
 
 # ----------------------------------------------------------------------------- the oracle on the CPU
-def oracle_unit_job(w, K, V, Q):
-    """One unit's whole job on the CPU oracle: prefill clustering, then every
-    decode step (incremental clustering every m steps, score, select, sparse
-    attention).  Returns (prefill seconds, decode seconds)."""
-    import oracle.clusterkv as ck
-    t0 = time.perf_counter()
-    st = ck.cluster_prefill(K, w.L, w.C, iters=w.iters, operand="bf16")
-    t1 = time.perf_counter()
-    end = w.L
-    for t in range(w.decode_steps):
-        if t > 0 and t % w.m == 0:
-            inc = ck.cluster_incremental(K, end, w.m, w.c_plus, iters=w.iters, operand="bf16")
-            st = ck.append_clusters(st, inc)
-            end += w.m
-        q = Q[t]
-        idx, _ = ck.select(ck.score(q, st["mu"]), st["sizes"], st["offsets"], st["perm"], w.B)
-        ck.sparse_attention(q, K, V, ck.attention_tokens(w.sinks, end, w.L + t + 1, idx))
-    t2 = time.perf_counter()
-    return t1 - t0, t2 - t1
+def oracle_jobs(w, n_units=None, device_tensors=None):
+    """The C++ oracle (float64, oracle/clusterkv_ref.cpp) on whole jobs of the
+    first n_units units (default: one per host core), all at once on a pool of
+    std::threads (one unit per thread): prefill clustering, then every decode
+    step (incremental clustering every m steps, score, select, sparse
+    attention).  Units are independent, so the workload's job time is the
+    measured wall time times units / n_units (an extrapolation, stated)."""
+    import oracle.cpp as cc
+    threads = os.cpu_count() or 1
+    n_units = min(w.units, n_units or threads)
+    units = list(range(n_units))
+    T = w.decode_steps
+    if device_tensors is not None:
+        K, V, Q = device_tensors
+        Ks = [K[u].double().cpu().numpy() for u in units]
+        Vs = [V[u].double().cpu().numpy() for u in units]
+        Qs = [Q[:T, u].double().cpu().numpy() for u in units]
+    else:
+        Kt, Vt = synth.make_kv(w, units=units)
+        Qt = synth.make_queries(w, T, units=units)
+        Ks = [Kt[i].double().numpy() for i in range(n_units)]
+        Vs = [Vt[i].double().numpy() for i in range(n_units)]
+        Qs = [Qt[:, i].double().numpy() for i in range(n_units)]
+    operand = "bf16" if w.dtype == "bf16" else "f64"
 
+    def run():
+        t0 = time.perf_counter()
+        _, times = cc.unit_jobs(Ks, Vs, Qs, w.L, w.C, w.B, iters=w.iters, m=w.m, c_plus=w.c_plus, sinks=w.sinks,
+                                operand=operand, threads=threads)
+        wall = time.perf_counter() - t0
+        job_s = wall * w.units / n_units
+        return {"wall_s": wall, "job_s": job_s, "tokens_per_s": w.batch * T / job_s,
+                "prefill_s_per_unit": float(times[:, 0].mean()), "decode_s_per_unit": float(times[:, 1].mean())}
 
-def oracle_sample(w, budget_s, device_tensors=None):
-    """Time the oracle on whole-unit jobs until `budget_s` seconds are spent
-    (at least one unit); scale to the full workload (units are independent)."""
-    times = []
-    t_start = time.perf_counter()
-    u = 0
-    while u < w.units and (u == 0 or time.perf_counter() - t_start < budget_s):
-        if device_tensors is not None:
-            K, V, Q = device_tensors
-            Ku, Vu, Qu = (x.double().cpu().numpy() for x in (K[u], V[u], Q[:, u]))
-        else:
-            Kt, Vt = synth.make_kv(w, units=[u])
-            Qt = synth.make_queries(w, w.decode_steps, units=[u])
-            Ku, Vu, Qu = Kt[0].double().numpy(), Vt[0].double().numpy(), Qt[:, 0].double().numpy()
-        times.append(oracle_unit_job(w, Ku, Vu, Qu))
-        u += 1
-    pre = statistics.mean(t[0] for t in times)
-    dec = statistics.mean(t[1] for t in times)
-    job_s = (pre + dec) * w.units
-    return {"tokens_per_s": w.batch * w.decode_steps / job_s, "prefill_s_per_unit": pre, "decode_s_per_unit": dec,
-            "units": len(times), "job_s": job_s}
+    return run, n_units, min(threads, n_units)
 
 
 def cpu_threads():
+    """Threads of the BLAS pool numpy would use (reported beside the core count)."""
     try:
         from threadpoolctl import threadpool_info
         n = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
@@ -834,24 +906,25 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        steps = []
-        sample_desc = None
-        for i in range(args.warmup + args.steps):
-            r = oracle_sample(w, 0.0)
-            if i >= args.warmup:
-                steps.append(r)
-            sample_desc = (f"one unit's whole job per step (prefill clustering of {w.L - w.sinks} keys "
-                           f"+ {w.decode_steps} decode steps), scaled x{w.units} units")
-        v = statistics.mean(r["tokens_per_s"] for r in steps)
-        cores = cpu_threads()
+        # each step: the C++ oracle on the whole jobs of one unit per host core,
+        # run at once and timed as they run; the workload's job time is that
+        # wall time times units / sampled units (reported as an extrapolation)
+        run, n_units, threads = oracle_jobs(w)
+        runs = [run() for _ in range(args.warmup + args.steps)][args.warmup:]
+        sample_desc = (f"{n_units} units' whole jobs per step (prefill clustering of {w.L - w.sinks} keys + "
+                       f"{w.decode_steps} decode steps each), one unit per thread, extrapolated "
+                       f"x{w.units}/{n_units} units")
+        v = statistics.mean(r["tokens_per_s"] for r in runs)
         line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup,
-                "ms_per_step": 1000 * statistics.mean(r["job_s"] for r in steps),
+                "ms_per_step": 1000 * statistics.mean(r["wall_s"] for r in runs),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic", "config": cfg,
-                "kmeans_ms_per_layer": 1000 * statistics.mean(r["prefill_s_per_unit"] for r in steps) * w.kv_heads * w.batch,
-                "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                                 "sample": sample_desc},
+                "extrapolated_job_s": statistics.mean(r["job_s"] for r in runs),
+                "kmeans_ms_per_layer": 1000 * statistics.mean(r["prefill_s_per_unit"] for r in runs) * w.kv_heads
+                                       * w.batch,
+                "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": threads, "host_cores": os.cpu_count(),
+                                 "kind": "oracle (C++, float64, std::thread pool)", "sample": sample_desc},
                 "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
@@ -865,73 +938,73 @@ def main():
     step_ms, prefill_ms, decode_ms = max_over_ranks([step_ms, prefill_ms, decode_ms], world)
     T = w.decode_steps
     value = job_value(world, T, step_ms, w.batch)
-    if r["one_call"]:
-        # one ckv_decode_step call per step: its launch window covers the whole
-        # step; its bytes are those of the whole step
-        step_gbs = r["step_bytes_per_launch"] / (r["step_launch_ms"] / 1000.0) / 1e9
-        roofline = {"bound": "hbm", "kernel": "score_kernel + sel_kernel + attn_mma_kernel + attn_mma_combine_kernel "
-                                              "(one ckv_decode_step: scoring, selection, gather, split-K "
-                                              "attention)",
-                    "achieved": step_gbs, "peak": hbm, "unit": "GB/s", "frac": step_gbs / hbm,
-                    "traffic": (STEP_TRAFFIC_PER_ALG_BYTE * r["step_bytes_per_launch"]
-                                if STEP_TRAFFIC_PER_ALG_BYTE else None),
-                    "traffic_source": STEP_TRAFFIC_SOURCE,
-                    "bytes_per_launch": r["step_bytes_per_launch"],
-                    "launch_us": 1000.0 * r["step_launch_ms"], "peak_kind": peak_kind,
-                    "timing": "CUDA events around the decode-step launch of every 16th decode step, inside "
-                              "the timed graph"}
-    else:
-        attn_gbs = r["attn_bytes_per_launch"] / (r["attn_ms"] / 1000.0) / 1e9
-        roofline = {"bound": "hbm", "kernel": "attn_mma_kernel + attn_mma_combine_kernel (gather + split-K "
-                                              "attention)",
-                    "achieved": attn_gbs, "peak": hbm, "unit": "GB/s", "frac": attn_gbs / hbm,
-                    "traffic": (ATTN_TRAFFIC_PER_ALG_BYTE * r["attn_bytes_per_launch"]
-                                if ATTN_TRAFFIC_PER_ALG_BYTE else None),
-                    "traffic_source": ATTN_TRAFFIC_SOURCE,
-                    "bytes_per_launch": r["attn_bytes_per_launch"],
-                    "launch_us": 1000.0 * r["attn_ms"], "peak_kind": peak_kind,
-                    "timing": "CUDA events around the attention launch (+ its combine kernel) of "
-                              "every 16th decode step, inside the timed graph"}
-    decode_gbs = r["decode_bytes_per_step"] / (decode_ms / T / 1000.0) / 1e9
+    # the decode step over the timed region: the job's algorithmic bytes per
+    # step (scoring, selection, gather + attention, the appended row) over the
+    # mean step time (CUDA events on the decode stream around the replay of
+    # the whole decode loop, which holds no event of its own)
+    append_b = w.units * 2 * w.d * 2 * 2
+    step_bytes = r["decode_bytes_per_step"] + append_b
+    step_us = 1000.0 * decode_ms / T
+    decode_gbs = step_bytes / (step_us / 1e6) / 1e9
+    kernels = ("append_kv_kernel + score_kernel + step_kernel + step_combine_kernel (ckv_append_kv + "
+               "ckv_decode_step: scoring, selection + gather + split-K attention in one kernel, combine)"
+               if r["one_call"] else
+               "append_kv_kernel + score_kernel + sel_kernel + attn_mma_kernel + attn_mma_combine_kernel "
+               "(ckv_append_kv + ckv_select + ckv_sparse_decode_attn)")
+    traffic_ratio = STEP_TRAFFIC_PER_ALG_BYTE if r["one_call"] else None
+    roofline = {"bound": "hbm", "kernel": kernels, "achieved": decode_gbs, "peak": hbm, "unit": "GB/s",
+                "frac": decode_gbs / hbm, "traffic": traffic_ratio * step_bytes if traffic_ratio else None,
+                "traffic_source": STEP_TRAFFIC_SOURCE if r["one_call"] else "not captured for this path",
+                "bytes_per_launch": step_bytes, "launch_us": step_us, "peak_kind": peak_kind,
+                "timing": "mean decode step of the timed region: CUDA events around each replay of the "
+                          f"{T}-step decode graph (incremental clustering included), on the decode stream"}
+    st = r["step_timing"]
+    iso_gbs = st["bytes_per_step"] / (st["step_us"] / 1e6) / 1e9
+    isolated = {"achieved": iso_gbs, "peak": hbm, "unit": "GB/s", "frac": iso_gbs / hbm,
+                "bytes_per_step": st["bytes_per_step"], "step_us": st["step_us"], "pending": st["pending"],
+                "timing": st["what"]}
+    if "attn_us" in st:
+        a_gbs = st["attn_bytes"] / (st["attn_us"] / 1e6) / 1e9
+        isolated["attention_alone"] = {"kernel": "attn_mma_kernel + attn_mma_combine_kernel", "us": st["attn_us"],
+                                       "bytes": st["attn_bytes"], "achieved": a_gbs, "frac": a_gbs / hbm}
     kflops, kbytes = kmeans_flops_bytes(w)
     assign_flops = kflops / w.iters
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
+        "roofline": roofline,
         "decode_tokens_per_s": world * w.batch * T / (decode_ms / 1000.0),
         "kmeans_ms_per_layer": prefill_ms * w.kv_heads / w.units,
-        "decode_step_us": 1000.0 * decode_ms / T,
-        "decode_roofline": {"bound": "hbm", "achieved": decode_gbs, "peak": hbm, "unit": "GB/s",
-                            "frac": decode_gbs / hbm, "bytes_per_step": r["decode_bytes_per_step"],
-                            "peak_kind": peak_kind},
+        "decode_step_us": step_us,
+        "decode_step_isolated": isolated,
         "kmeans_roofline": {"tflops": kflops / (prefill_ms / 1000.0) / 1e12,
                             "peak_tflops": meas.get("bf16_tflops_sustained", 1700.0),
                             "bytes_gbs": kbytes / (prefill_ms / 1000.0) / 1e9},
-        "roofline": roofline,
         "assign_roofline": {"bound": "tensor", "kernel": "assign_tc_kernel",
                             "achieved": assign_flops / (r["assign_ms"] / 1000.0) / 1e12,
                             "peak": meas.get("bf16_tflops", 1900.0), "unit": "TFLOP/s",
                             "frac": assign_flops / (r["assign_ms"] / 1000.0) / 1e12 / meas.get("bf16_tflops", 1900.0),
                             "launch_us": 1000.0 * r["assign_ms"], "peak_kind": peak_kind + " (burst: timed alone)"},
         "recall": r["recall"],
-        "reuse": r["reuse"],
-        "channel_prescore": r["channel_prescore"],
-        "full_kv": dict(r["full_kv"], decode_speedup=r["full_kv"]["attention_us"] / (1000.0 * decode_ms / T)),
-        "quest": r["quest"],
         "phase_ms": {"prefill_clustering": prefill_ms, "decode_loop": decode_ms},
-        "per_launch_us": ({"decode_step": 1000.0 * r["step_launch_ms"]} if r["one_call"] else
-                          {"select": 1000.0 * r["select_ms"], "attention": 1000.0 * r["attn_ms"]}),
         "gpu_launches": r["launches"], "clocks": r["clocks"],
     }
+    for k in ("reuse", "channel_prescore", "quest", "async_clustering"):
+        if k in r:
+            line[k] = r[k]
+    if "full_kv" in r:
+        line["full_kv"] = dict(r["full_kv"], decode_speedup=r["full_kv"]["attention_us"] / step_us)
     if "e2e" in r:
         line["e2e"] = r["e2e"]
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cb = oracle_sample(w, args.cpu_seconds, r["tensors"])
-        line["cpu_baseline"] = {"value": cb["tokens_per_s"], "unit": "tokens/s", "cores": cpu_threads(),
-                                "kind": "oracle",
-                                "sample": f"{cb['units']} unit(s)' whole job (prefill clustering + "
-                                          f"{T} decode steps) on the host, scaled x{w.units} units"}
+        run, n_units, threads = oracle_jobs(w, device_tensors=r["tensors"])
+        cb = run()
+        line["cpu_baseline"] = {"value": cb["tokens_per_s"], "unit": "tokens/s", "cores": threads,
+                                "host_cores": os.cpu_count(), "kind": "oracle (C++, float64, std::thread pool)",
+                                "sample": f"{n_units} units' whole jobs (prefill clustering + {T} decode steps each) "
+                                          f"on {threads} threads in {cb['wall_s']:.1f} s, extrapolated "
+                                          f"x{w.units}/{n_units} units"}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

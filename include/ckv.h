@@ -314,19 +314,21 @@ ckv_status ckv_channel_prescore(ckv_ctx* ctx, const void* q, int32_t q_dtype, co
  * count and out have the layouts given at the top of this file (K and V with
  * max_len rows per unit).  dev_err is an optional device int32 (NULL = none)
  * that receives CKV_DEV_* codes.
- * Scratch: the split partials and per-unit counters live in one fixed 8 MiB
- * device array inside the library (held on every device that loads the
- * library until the process exits).  A call needs
+ * Scratch: the split partials live in one fixed 8 MiB device array inside
+ * the library (held on every device that loads the library until the process
+ * exits).  A call needs
  *   units * ceil((sinks + cur_len - clustered_end + B) / R) * g * 130 * 4
- * bytes (rounded up to 256) + 4 * units bytes, where R is the rows of one
- * attention work item: 16 for bf16, 64 for fp32 with g <= 4 and 32 for fp32
- * with g = 8; larger calls return
+ * bytes, where R is the rows of one attention work item: 16 for bf16, 64 for
+ * fp32 with g <= 4 and 32 for fp32 with g = 8; larger calls return
  * CKV_ERR_CAPACITY before launching anything.  The first call on each device
- * looks the array's device address up (cudaGetSymbolAddress), so make that
- * first call before any stream capture.  Every call reuses the same array
- * (the counters are cleared on the stream at the start of each call), so
- * calls that can overlap on the GPU (different streams without ordering)
- * race and must not be issued.  Errors: CKV_ERR_ARG, CKV_ERR_DTYPE,
+ * looks the array's device address up (cudaGetSymbolAddress) in that device's
+ * primary context (the one the CUDA runtime uses) and keeps it: make that
+ * first call before any stream capture, and do not use the entry point across
+ * a cudaDeviceReset (the cached address would be stale).  Every call reuses
+ * the same array and overwrites what the previous call left in it (nothing is
+ * read before the same call writes it), so calls that can overlap on the GPU
+ * (different streams without ordering) race and must not be issued.
+ * Errors: CKV_ERR_ARG, CKV_ERR_DTYPE,
  * CKV_ERR_ALIGN, CKV_ERR_CAPACITY, CKV_ERR_CUDA. */
 ckv_status ckv_sparse_decode_attn_noalloc(const void* q, int32_t q_dtype, const void* K,
                                           const void* V, const int32_t* idx, const int32_t* count,
@@ -353,6 +355,24 @@ ckv_status ckv_export_clusters(ckv_ctx* ctx, float* mu, void* mu_hat, int32_t* s
 ckv_status ckv_import_clusters(ckv_ctx* ctx, int32_t n_clusters, int32_t clustered_end,
                                const float* mu, const int32_t* sizes, const int32_t* offsets,
                                const int32_t* perm, void* stream);
+
+/* Failure detection.  Every wait inside the library's kernels (an mbarrier
+ * phase, a flag another warp sets) is bounded: after `cycles` SM clock cycles
+ * (default 2e9, about one second at 2 GHz) the waiting warp gives up, records
+ * CKV_DEV_TIMEOUT in the device error word, the kernel lets the copies and
+ * tensor-core operations it already started complete (each of those waits
+ * bounded the same way), releases its tensor memory and returns; the context
+ * stays usable.  ckv_set_wait_limit sets that limit for this context's later
+ * launches (1 <= cycles <= 4e9).  stall = 1 makes the next launches of three
+ * kernels wait once on something nothing ever completes, so that their
+ * failure path runs: the tensor-core K-means assignment (bf16 keys), the fp32
+ * sparse attention, and the one-kernel decode step of ckv_decode_step (whose
+ * selections are then never published: its attention warps give up and treat
+ * every selection as empty, and idx / count are not written).  stall = 0
+ * restores normal operation.  This exists to test failure detection (see
+ * ckv_get_device_error) without faulting or hanging a GPU.
+ * Errors: CKV_ERR_ARG. */
+ckv_status ckv_set_wait_limit(ckv_ctx* ctx, int64_t cycles, int32_t stall);
 
 /* Synchronises the context's last stream and reads then clears the device
  * error word (CKV_DEV_*). */

@@ -45,6 +45,7 @@ SIGNATURES = {
     "ckv_export_clusters": ([_P, _P, _P, _P, _P, _P, _P], _I),
     "ckv_import_clusters": ([_P, _I, _I, _P, _P, _P, _P, _P], _I),
     "ckv_get_device_error": ([_P, ctypes.POINTER(_I)], _I),
+    "ckv_set_wait_limit": ([_P, ctypes.c_int64, _I], _I),
     "ckv_sparse_decode_attn_noalloc": ([_P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P], _I),
 }
 
@@ -221,6 +222,11 @@ class Context:
         _check(lib().ckv_import_clusters(self.handle, n_clusters, clustered_end, ptr(mu), ptr(sizes),
                                          ptr(offsets), ptr(perm), _stream(stream)),
                "ckv_import_clusters")
+
+    def set_wait_limit(self, cycles: int = 2_000_000_000, stall: bool = False):
+        """Bounded-wait limit of this context's kernels, and the failure
+        detection test switch (see ckv_set_wait_limit)."""
+        _check(lib().ckv_set_wait_limit(self.handle, int(cycles), 1 if stall else 0), "ckv_set_wait_limit")
 
     def device_error(self) -> int:
         v = ctypes.c_int32()

@@ -34,7 +34,8 @@ cudaError_t alloc(T** p, size_t count) {
 void free_all(ckv_ctx* c) {
     void* ptrs[] = {c->mu32,   c->mu_s == c->mu32 ? nullptr : c->mu_s, c->mu_hat, c->sizes,
                     c->offsets, c->perm, c->labels, c->chunk_cnt, c->task_off, c->task_cl,
-                    c->seg_part, c->scores, c->attn_part, c->attn_cnt, c->dev_err, c->assign_best};
+                    c->seg_part, c->scores, c->attn_part, c->dev_err, c->assign_best,
+                    c->sel_flag};
     for (void* p : ptrs)
         if (p) cudaFree(p);
     if (c->pend_done) cudaEventDestroy(c->pend_done);
@@ -74,6 +75,7 @@ const char* ckv_status_str(int32_t status) {
 int32_t ckv_version(void) { return VERSION; }
 
 ckv_status ckv_create(const ckv_config* cfg, ckv_ctx** out) {
+    CKV_TRACE("ckv_create");
     if (!out) return CKV_ERR_ARG;
     *out = nullptr;
     if (!cfg) return CKV_ERR_ARG;
@@ -103,6 +105,10 @@ ckv_status ckv_create(const ckv_config* cfg, ckv_ctx** out) {
     c->max_tasks = ceil_div(c->ntok, SEG_ROWS) + c->cmax;
     c->attn_rows = cfg->sinks + cfg->max_budget + 2 * cfg->m;
     c->max_splits = ceil_div(c->attn_rows, attention_rows_per_split(cfg->kv_dtype, cfg->g));
+    if (c->max_splits < STEP_MIN_SLOTS) c->max_splits = STEP_MIN_SLOTS;
+    c->wait_limit = WAIT_LIMIT;
+    c->stall = 0;
+    c->sel_flag_dirty = false;
     c->elem = cfg->kv_dtype == CKV_BF16 ? 2 : 4;
     c->last_stream = nullptr;
     c->pend_m = 0;
@@ -128,15 +134,16 @@ ckv_status ckv_create(const ckv_config* cfg, ckv_ctx** out) {
     ok = ok && alloc(&c->seg_part, U * c->max_tasks * D) == cudaSuccess;
     ok = ok && alloc(&c->scores, U * c->cmax) == cudaSuccess;
     ok = ok && alloc(&c->attn_part, U * c->max_splits * cfg->g * (D + 2)) == cudaSuccess;
-    ok = ok && alloc(&c->attn_cnt, U) == cudaSuccess;
     ok = ok && alloc(&c->dev_err, 1) == cudaSuccess;
+    ok = ok && alloc(&c->sel_flag, U) == cudaSuccess;
     ok = ok && cudaEventCreateWithFlags(&c->pend_done, cudaEventDisableTiming) == cudaSuccess;
     if (cfg->kv_dtype == CKV_BF16 && c->cmax_pad > MAX_ASSIGN_CPAD)
         ok = ok && alloc(&c->assign_best, U * c->ntok) == cudaSuccess;
     if (ok) {
         const size_t hat = U * (size_t)c->cmax_pad * D * c->elem;
-        ok = cudaMemset(c->mu_hat, 0, hat) == cudaSuccess && cudaMemset(c->attn_cnt, 0, U * 4) == cudaSuccess &&
+        ok = cudaMemset(c->mu_hat, 0, hat) == cudaSuccess &&
              cudaMemset(c->dev_err, 0, 4) == cudaSuccess && cudaMemset(c->sizes, 0, U * c->cmax * 4) == cudaSuccess &&
+             cudaMemset(c->sel_flag, 0, U * 4) == cudaSuccess &&
              cudaDeviceSynchronize() == cudaSuccess;
     }
     if (!ok) {
@@ -150,6 +157,7 @@ ckv_status ckv_create(const ckv_config* cfg, ckv_ctx** out) {
 }
 
 ckv_status ckv_destroy(ckv_ctx* ctx) {
+    CKV_TRACE("ckv_destroy");
     if (!ctx) return CKV_ERR_ARG;
     cudaDeviceSynchronize();
     free_all(ctx);
@@ -158,6 +166,7 @@ ckv_status ckv_destroy(ckv_ctx* ctx) {
 }
 
 ckv_status ckv_cluster_prefill(ckv_ctx* ctx, const void* K, int32_t L, int32_t n_clusters, void* stream) {
+    CKV_TRACE("ckv_cluster_prefill");
     ckv_status st = check_kv(ctx, K);
     if (st != CKV_OK) return st;
     if ((st = check_L(ctx, L)) != CKV_OK) return st;
@@ -188,6 +197,7 @@ ckv_status ckv_cluster_prefill(ckv_ctx* ctx, const void* K, int32_t L, int32_t n
 
 ckv_status ckv_cluster_incremental(ckv_ctx* ctx, const void* K, int32_t start, int32_t m, int32_t c_plus,
                                    void* stream) {
+    CKV_TRACE("ckv_cluster_incremental");
     ckv_status st = check_kv(ctx, K);
     if (st != CKV_OK) return st;
     if (ctx->pend_m > 0) return CKV_ERR_STATE;
@@ -207,6 +217,7 @@ ckv_status ckv_cluster_incremental(ckv_ctx* ctx, const void* K, int32_t start, i
 
 ckv_status ckv_cluster_incremental_begin(ckv_ctx* ctx, const void* K, int32_t start, int32_t m, int32_t c_plus,
                                          void* stream) {
+    CKV_TRACE("ckv_cluster_incremental_begin");
     ckv_status st = check_kv(ctx, K);
     if (st != CKV_OK) return st;
     if (ctx->pend_m > 0) return CKV_ERR_STATE;
@@ -228,6 +239,7 @@ ckv_status ckv_cluster_incremental_begin(ckv_ctx* ctx, const void* K, int32_t st
 }
 
 ckv_status ckv_cluster_incremental_commit(ckv_ctx* ctx, void* stream) {
+    CKV_TRACE("ckv_cluster_incremental_commit");
     if (!ctx) return CKV_ERR_ARG;
     if (ctx->pend_m <= 0) return CKV_ERR_STATE;
     cudaStream_t s = (cudaStream_t)stream;
@@ -241,6 +253,7 @@ ckv_status ckv_cluster_incremental_commit(ckv_ctx* ctx, void* stream) {
 }
 
 ckv_status ckv_kmeans_assign(ckv_ctx* ctx, const void* K, int32_t L, int32_t* labels, void* stream) {
+    CKV_TRACE("ckv_kmeans_assign");
     ckv_status st = check_kv(ctx, K);
     if (st != CKV_OK) return st;
     if ((st = check_L(ctx, L)) != CKV_OK) return st;
@@ -254,6 +267,7 @@ ckv_status ckv_kmeans_assign(ckv_ctx* ctx, const void* K, int32_t L, int32_t* la
 }
 
 ckv_status ckv_kmeans_update(ckv_ctx* ctx, const void* K, int32_t L, const int32_t* labels, void* stream) {
+    CKV_TRACE("ckv_kmeans_update");
     ckv_status st = check_kv(ctx, K);
     if (st != CKV_OK) return st;
     if ((st = check_L(ctx, L)) != CKV_OK) return st;
@@ -270,6 +284,7 @@ ckv_status ckv_kmeans_update(ckv_ctx* ctx, const void* K, int32_t L, const int32
 }
 
 ckv_status ckv_score(ckv_ctx* ctx, const void* q, int32_t q_dtype, float* scores, void* stream) {
+    CKV_TRACE("ckv_score");
     if (!ctx || !q || !scores) return CKV_ERR_ARG;
     if (q_dtype != ctx->cfg.kv_dtype) return CKV_ERR_DTYPE;
     if (!aligned16(q)) return CKV_ERR_ALIGN;
@@ -281,6 +296,7 @@ ckv_status ckv_score(ckv_ctx* ctx, const void* q, int32_t q_dtype, float* scores
 
 ckv_status ckv_select_scored(ckv_ctx* ctx, const float* scores, int32_t B, int32_t* idx, int32_t* count,
                              void* stream) {
+    CKV_TRACE("ckv_select_scored");
     if (!ctx || !scores || !idx || !count) return CKV_ERR_ARG;
     if (B < 0) return CKV_ERR_ARG;
     if (B > ctx->cfg.max_budget) return CKV_ERR_CAPACITY;
@@ -293,6 +309,7 @@ ckv_status ckv_select_scored(ckv_ctx* ctx, const float* scores, int32_t B, int32
 
 ckv_status ckv_select(ckv_ctx* ctx, const void* q, int32_t q_dtype, int32_t B, int32_t* idx, int32_t* count,
                       void* stream) {
+    CKV_TRACE("ckv_select");
     if (!ctx || !q || !idx || !count) return CKV_ERR_ARG;
     if (q_dtype != ctx->cfg.kv_dtype) return CKV_ERR_DTYPE;
     if (!aligned16(q)) return CKV_ERR_ALIGN;
@@ -308,6 +325,7 @@ ckv_status ckv_select(ckv_ctx* ctx, const void* q, int32_t q_dtype, int32_t B, i
 ckv_status ckv_sparse_decode_attn(ckv_ctx* ctx, const void* q, int32_t q_dtype, const void* K, const void* V,
                                   const int32_t* idx, const int32_t* count, int32_t B, int32_t cur_len, float* out,
                                   void* stream) {
+    CKV_TRACE("ckv_sparse_decode_attn");
     if (!ctx || !q || !K || !V || !idx || !count || !out) return CKV_ERR_ARG;
     if (q_dtype != ctx->cfg.kv_dtype) return CKV_ERR_DTYPE;
     if (!aligned16(q) || !aligned16(K) || !aligned16(V) || !aligned16(out)) return CKV_ERR_ALIGN;
@@ -320,12 +338,14 @@ ckv_status ckv_sparse_decode_attn(ckv_ctx* ctx, const void* q, int32_t q_dtype, 
     ctx->last_stream = s;
     cudaError_t e = launch_attention(q, K, V, idx, count, ctx->cfg.units, ctx->cfg.g, ctx->cfg.kv_dtype,
                                      ctx->cfg.max_len, ctx->cfg.sinks, ctx->clustered_end, cur_len, B, out,
-                                     ctx->attn_part, ctx->attn_cnt, ctx->max_splits, ctx->dev_err, ctx->num_sms, s);
+                                     ctx->attn_part, ctx->max_splits, ctx->dev_err, ctx->num_sms,
+                                     ctx->wait_limit, ctx->stall, s);
     return cuda_status(e);
 }
 
 ckv_status ckv_decode_step(ckv_ctx* ctx, const void* q, int32_t q_dtype, const void* K, const void* V, int32_t B,
                            int32_t cur_len, int32_t* idx, int32_t* count, float* out, void* stream) {
+    CKV_TRACE("ckv_decode_step");
     if (!ctx || !q || !K || !V || !idx || !count || !out) return CKV_ERR_ARG;
     if (q_dtype != ctx->cfg.kv_dtype) return CKV_ERR_DTYPE;
     if (!aligned16(q) || !aligned16(K) || !aligned16(V) || !aligned16(out)) return CKV_ERR_ALIGN;
@@ -337,17 +357,32 @@ ckv_status ckv_decode_step(ckv_ctx* ctx, const void* q, int32_t q_dtype, const v
     if (ctx->n_clusters > MAX_SELECT_CLUSTERS) return CKV_ERR_UNIMPLEMENTED;
     cudaStream_t s = (cudaStream_t)stream;
     ctx->last_stream = s;
+    if (step_supported(ctx->cfg.kv_dtype, ctx->cfg.g, ctx->n_clusters, ctx->cfg.units, ctx->num_sms)) {
+        // scoring, then one kernel that selects and attends (its attention warps
+        // stream the sinks and pending rows while its selector warps rank the
+        // clusters), then the combine
+        cudaError_t e = cudaSuccess;
+        if (ctx->sel_flag_dirty) e = cudaMemsetAsync(ctx->sel_flag, 0, (size_t)ctx->cfg.units * 4, s);
+        if (e == cudaSuccess) e = launch_score(ctx, q, ctx->n_clusters, ctx->scores, ctx->cmax, s, true);
+        if (e == cudaSuccess) {
+            ctx->sel_flag_dirty = false;
+            e = launch_step(ctx, q, K, V, ctx->n_clusters, B, cur_len, idx, count, out, ctx->wait_limit, s);
+            if (e != cudaSuccess) ctx->sel_flag_dirty = true;
+        }
+        return cuda_status(e);
+    }
     // selection, then attention (a dependent launch: it is scheduled while the
     // selection drains and waits for it on the device)
     cudaError_t e = launch_select(ctx, q, nullptr, 0, ctx->n_clusters, B, idx, count, s);
     if (e == cudaSuccess)
         e = launch_attention(q, K, V, idx, count, ctx->cfg.units, ctx->cfg.g, ctx->cfg.kv_dtype, ctx->cfg.max_len,
-                             ctx->cfg.sinks, ctx->clustered_end, cur_len, B, out, ctx->attn_part, ctx->attn_cnt,
-                             ctx->max_splits, ctx->dev_err, ctx->num_sms, s);
+                             ctx->cfg.sinks, ctx->clustered_end, cur_len, B, out, ctx->attn_part,
+                             ctx->max_splits, ctx->dev_err, ctx->num_sms, ctx->wait_limit, ctx->stall, s);
     return cuda_status(e);
 }
 
 ckv_status ckv_get_info(ckv_ctx* ctx, ckv_info* info) {
+    CKV_TRACE("ckv_get_info");
     if (!ctx || !info) return CKV_ERR_ARG;
     info->n_clusters = ctx->n_clusters;
     info->prefill_clusters = ctx->prefill_clusters;
@@ -358,6 +393,7 @@ ckv_status ckv_get_info(ckv_ctx* ctx, ckv_info* info) {
 
 ckv_status ckv_export_clusters(ckv_ctx* ctx, float* mu, void* mu_hat, int32_t* sizes, int32_t* offsets,
                                int32_t* perm, void* stream) {
+    CKV_TRACE("ckv_export_clusters");
     if (!ctx) return CKV_ERR_ARG;
     const int C = ctx->n_clusters;
     if (C <= 0) return CKV_ERR_STATE;
@@ -386,6 +422,7 @@ ckv_status ckv_export_clusters(ckv_ctx* ctx, float* mu, void* mu_hat, int32_t* s
 
 ckv_status ckv_import_clusters(ckv_ctx* ctx, int32_t n_clusters, int32_t clustered_end, const float* mu,
                                const int32_t* sizes, const int32_t* offsets, const int32_t* perm, void* stream) {
+    CKV_TRACE("ckv_import_clusters");
     if (!ctx || !mu) return CKV_ERR_ARG;
     if (n_clusters < 1) return CKV_ERR_ARG;
     if (n_clusters > ctx->cmax) return CKV_ERR_CAPACITY;
@@ -421,7 +458,17 @@ ckv_status ckv_import_clusters(ckv_ctx* ctx, int32_t n_clusters, int32_t cluster
     return CKV_OK;
 }
 
+ckv_status ckv_set_wait_limit(ckv_ctx* ctx, int64_t cycles, int32_t stall) {
+    CKV_TRACE("ckv_set_wait_limit");
+    if (!ctx) return CKV_ERR_ARG;
+    if (cycles < 1 || cycles > MAX_WAIT_LIMIT || (stall != 0 && stall != 1)) return CKV_ERR_ARG;
+    ctx->wait_limit = cycles;
+    ctx->stall = stall;
+    return CKV_OK;
+}
+
 ckv_status ckv_get_device_error(ckv_ctx* ctx, int32_t* code) {
+    CKV_TRACE("ckv_get_device_error");
     if (!ctx || !code) return CKV_ERR_ARG;
     cudaError_t e = cudaStreamSynchronize(ctx->last_stream);
     int32_t v = 0;

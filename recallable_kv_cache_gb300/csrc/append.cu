@@ -13,6 +13,7 @@
 #include <stdint.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace ckv {
 namespace {
@@ -28,6 +29,9 @@ __global__ void __launch_bounds__(APPEND_THREADS) append_kv_kernel(const uint4* 
                                                                    size_t n_chunks, size_t span, size_t dst_stride,
                                                                    size_t dst_off, uint4* __restrict__ K,
                                                                    uint4* __restrict__ V) {
+    // the caller's previous kernels may still read or write the caches
+    ptx::grid_dependency_wait();
+    ptx::allow_dependent_launch();
     const int u = blockIdx.y;
     const size_t c0 = (size_t)blockIdx.x * span;
     const size_t c1 = c0 + span < n_chunks ? c0 + span : n_chunks;
@@ -77,8 +81,10 @@ extern "C" ckv_status ckv_append_kv(const void* k_src, const void* v_src, int32_
     const size_t span = (size_t)APPEND_THREADS * APPEND_UNROLL * 16;
     const size_t blocks = (n_chunks + span - 1) / span;
     if (blocks > 0x7fffffffu || units > 65535) return CKV_ERR_ARG;
-    append_kv_kernel<<<dim3((unsigned)blocks, units), APPEND_THREADS, 0, (cudaStream_t)stream>>>(
+    CKV_TRACE("ckv_append_kv");
+    const cudaError_t e = launch_dependent(
+        append_kv_kernel, dim3((unsigned)blocks, units), dim3(APPEND_THREADS), 0, (cudaStream_t)stream,
         static_cast<const uint4*>(k_src), static_cast<const uint4*>(v_src), (size_t)src_len * cpr, n_chunks, span,
         (size_t)max_len * cpr, (size_t)pos * cpr, static_cast<uint4*>(K), static_cast<uint4*>(V));
-    return cudaGetLastError() == cudaSuccess ? CKV_OK : CKV_ERR_CUDA;
+    return e == cudaSuccess ? CKV_OK : CKV_ERR_CUDA;
 }

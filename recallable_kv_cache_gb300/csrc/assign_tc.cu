@@ -61,6 +61,8 @@ struct AssignArgs {
     int32_t* labels;
     float* best;        // [units][n] running maxima between passes (npass > 1)
     int32_t* dev_err;
+    long long wait_limit;  // SM cycles before a wait gives up
+    int stall;          // failure detection test: the MMA issuer first waits on a barrier nothing completes
 };
 
 struct __align__(8) Bars {
@@ -74,13 +76,15 @@ struct __align__(8) Bars {
     uint64_t part_free[4];   // ... and consumed
     float xbest[4][EPI_PER_Q - 1][32];
     int xarg[4][EPI_PER_Q - 1][32];
+    uint64_t never;          // no thread or copy ever arrives (failure detection test)
+    uint64_t drain;          // completion of every MMA the issuer started, after an abort
     uint32_t tmem_base;
     int abort;
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Bars* bs,
-                                              int32_t* dev_err) {
-    if (ptx::mbar_wait(bar, parity, WAIT_LIMIT, &bs->abort)) return true;
+                                              int32_t* dev_err, long long limit) {
+    if (ptx::mbar_wait(bar, parity, limit, &bs->abort)) return true;
     if (atomicExch(&bs->abort, 1) == 0 && dev_err) atomicCAS(dev_err, 0, CKV_DEV_TIMEOUT);
     return false;
 }
@@ -115,6 +119,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             ptx::mbar_init(&bs->part_full[qq], EPI_PER_Q - 1);
             ptx::mbar_init(&bs->part_free[qq], 1);
         }
+        ptx::mbar_init(&bs->never, 1);
+        ptx::mbar_init(&bs->drain, 1);
         bs->abort = 0;
         ptx::fence_barrier_init();
     }
@@ -127,6 +133,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = bs->tmem_base;
 
+    int p_loads = 0, p_bloads = 0;  // copies the producer issued (for the drain after an abort)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
@@ -140,7 +147,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int ps = 0; ps < p.npass && alive; ++ps) {
                     const int prow = ps * p.pw;
                     const int rows = min(p.pw, p.cpad - prow);
-                    if (b_loads > 0 && !wait_or_abort(&bs->b_empty, (b_loads - 1) & 1, bs, p.dev_err)) {
+                    if (b_loads > 0 && !wait_or_abort(&bs->b_empty, (b_loads - 1) & 1, bs, p.dev_err, p.wait_limit)) {
                         alive = false;
                         break;
                     }
@@ -153,7 +160,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     for (int t = t0; t < t1; ++t, ++it) {
                         const int s = it % p.stages;
                         if (it >= p.stages &&
-                            !wait_or_abort(&bs->a_empty[s], ((it / p.stages) - 1) & 1, bs, p.dev_err)) {
+                            !wait_or_abort(&bs->a_empty[s], ((it / p.stages) - 1) & 1, bs, p.dev_err, p.wait_limit)) {
                             alive = false;
                             break;
                         }
@@ -166,6 +173,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 t0 = t1;
             }
+            p_loads = it;
+            p_bloads = b_loads;
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -174,6 +183,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint32_t b_base = ptx::smem_u32(Bm);
             int b_loads = 0, it = 0, item = 0;
             bool alive = true;
+            if (p.stall && !wait_or_abort(&bs->never, 0, bs, p.dev_err, p.wait_limit)) alive = false;
             for (int t0 = t_begin; t0 < t_end && alive;) {
                 const int u = t0 / p.tiles_per_unit;
                 const int t1 = min(t_end, (u + 1) * p.tiles_per_unit);
@@ -183,14 +193,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                     // the previous pass's centroid rows may be overwritten once
                     // every MMA issued so far has completed
                     if (b_loads > 0) ptx::mma_commit(&bs->b_empty);
-                    if (!wait_or_abort(&bs->b_full, b_loads & 1, bs, p.dev_err)) {
+                    if (!wait_or_abort(&bs->b_full, b_loads & 1, bs, p.dev_err, p.wait_limit)) {
                         alive = false;
                         break;
                     }
                     ++b_loads;
                     for (int t = t0; t < t1 && alive; ++t, ++it) {
                         const int s = it % p.stages;
-                        if (!wait_or_abort(&bs->a_full[s], (it / p.stages) & 1, bs, p.dev_err)) {
+                        if (!wait_or_abort(&bs->a_full[s], (it / p.stages) & 1, bs, p.dev_err, p.wait_limit)) {
                             alive = false;
                             break;
                         }
@@ -199,7 +209,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         for (int ch = 0; ch < nch; ++ch, ++item) {
                             const int slot = item & 1;
                             if (item >= 2 &&
-                                !wait_or_abort(&bs->tm_empty[slot], ((item >> 1) - 1) & 1, bs, p.dev_err)) {
+                                !wait_or_abort(&bs->tm_empty[slot], ((item >> 1) - 1) & 1, bs, p.dev_err, p.wait_limit)) {
                                 alive = false;
                                 break;
                             }
@@ -252,7 +262,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     for (int ch = 0; ch < nch; ++ch, ++item) {
                         const int slot = item & 1;
                         const bool ok = __all_sync(
-                            0xffffffffu, wait_or_abort(&bs->tm_full[slot], (item >> 1) & 1, bs, p.dev_err));
+                            0xffffffffu, wait_or_abort(&bs->tm_full[slot], (item >> 1) & 1, bs, p.dev_err, p.wait_limit));
                         if (!ok) {
                             alive = false;
                             break;
@@ -314,7 +324,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         }
                     if (sub > 0) {
                         if (ntile > 0 && !__all_sync(0xffffffffu, wait_or_abort(&bs->part_free[q], (ntile - 1) & 1,
-                                                                                 bs, p.dev_err))) {
+                                                                                 bs, p.dev_err, p.wait_limit))) {
                             alive = false;
                             break;
                         }
@@ -324,7 +334,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         if (lane == 0) ptx::mbar_arrive(&bs->part_full[q]);
                     } else {
                         if (!__all_sync(0xffffffffu,
-                                        wait_or_abort(&bs->part_full[q], ntile & 1, bs, p.dev_err))) {
+                                        wait_or_abort(&bs->part_full[q], ntile & 1, bs, p.dev_err, p.wait_limit))) {
                             alive = false;
                             break;
                         }
@@ -368,12 +378,24 @@ __global__ void __launch_bounds__(THREADS, 1)
     ptx::tc_fence_before();
     __syncthreads();
     if (bs->abort) {
-        // let copies / MMAs already issued drain before TMEM is released
-        const long long t0 = clock64();
-        while (clock64() - t0 < 20000000LL) {
+        // a wait gave up, so some copies or MMAs may not have been consumed:
+        // the producer waits (bounded) for the last phase of every stage and
+        // of the centroid panel it armed, the MMA issuer for every MMA it
+        // started, before the CTA's shared memory and TMEM are released
+        if (warp == 0 && lane == 0) {
+            for (int j = p_loads > p.stages ? p_loads - p.stages : 0; j < p_loads; ++j)
+                if (!ptx::mbar_wait(&bs->a_full[j % p.stages], (j / p.stages) & 1, p.wait_limit, nullptr) && p.dev_err)
+                    atomicCAS(p.dev_err, 0, CKV_DEV_TIMEOUT);
+            if (p_bloads > 0 && !ptx::mbar_wait(&bs->b_full, (p_bloads - 1) & 1, p.wait_limit, nullptr) && p.dev_err)
+                atomicCAS(p.dev_err, 0, CKV_DEV_TIMEOUT);
+        }
+        if (warp == 1 && lane == 0) {
+            ptx::mma_commit(&bs->drain);
+            if (!ptx::mbar_wait(&bs->drain, 0, p.wait_limit, nullptr) && p.dev_err) atomicCAS(p.dev_err, 0, CKV_DEV_TIMEOUT);
         }
     }
     if (warp == 1) {
+        __syncwarp();
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, 512);
     }
@@ -460,6 +482,8 @@ cudaError_t launch_assign_tc(const ckv_ctx* ctx, const void* K, int n, int C, in
     a.labels = labels;
     a.best = ctx->assign_best;
     a.dev_err = ctx->dev_err;
+    a.wait_limit = ctx->wait_limit;
+    a.stall = ctx->stall;
     cudaError_t e = cudaFuncSetAttribute(assign_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;

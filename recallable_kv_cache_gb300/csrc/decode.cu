@@ -555,8 +555,9 @@ struct AttnArgs {
     float qscale;
     float* out;
     float* part;
-    int32_t* counters;
     int32_t* dev_err;
+    long long wait_limit;  // SM cycles before a wait gives up
+    int stall;             // failure detection test: consumer warp 0 first waits on a barrier nothing completes
 };
 
 // Persistent, warp-specialised sparse decode attention.  Work items are
@@ -584,7 +585,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_kernel(const AttnArgs a) 
     int32_t* stok = reinterpret_cast<int32_t*>(psm + ATT_CW * RPI * NB * G);  // [STAGES][SR]
     T* sq = reinterpret_cast<T*>(stok + ATT_STAGES * SR);          // [STAGES][G][D]
     __shared__ int s_unit[ATT_STAGES], s_nrows[ATT_STAGES];
-    __shared__ __align__(8) uint64_t full[ATT_STAGES], empty[ATT_STAGES], red_full, red_free;
+    __shared__ __align__(8) uint64_t full[ATT_STAGES], empty[ATT_STAGES], red_full, red_free, never;
     __shared__ int abort_flag;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -599,6 +600,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_kernel(const AttnArgs a) 
         }
         ptx::mbar_init(&red_full, ATT_CW);
         ptx::mbar_init(&red_free, ATT_CW);
+        ptx::mbar_init(&never, 1);
         abort_flag = 0;
         ptx::fence_barrier_init();
     }
@@ -621,7 +623,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_kernel(const AttnArgs a) 
         for (int it = 0; it < nitems; ++it) {
             const int st = it % ATT_STAGES;
             if (it >= ATT_STAGES &&
-                !__all_sync(FULL, ptx::mbar_wait(&empty[st], ((it / ATT_STAGES) - 1) & 1, WAIT_LIMIT, &abort_flag))) {
+                !__all_sync(FULL, ptx::mbar_wait(&empty[st], ((it / ATT_STAGES) - 1) & 1, a.wait_limit, &abort_flag))) {
                 give_up();
                 break;
             }
@@ -739,7 +741,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_kernel(const AttnArgs a) 
             }
             // the previous merge has finished reading the exchange area
             if (flushes > 0 &&
-                !__all_sync(FULL, ptx::mbar_wait(&red_free, (flushes - 1) & 1, WAIT_LIMIT, &abort_flag)))
+                !__all_sync(FULL, ptx::mbar_wait(&red_free, (flushes - 1) & 1, a.wait_limit, &abort_flag)))
                 return false;
             float* rw = red + (size_t)w * PW;
             if (sub == 0) {
@@ -755,7 +757,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_kernel(const AttnArgs a) 
             }
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&red_full);
-            if (!__all_sync(FULL, ptx::mbar_wait(&red_full, flushes & 1, WAIT_LIMIT, &abort_flag)))
+            if (!__all_sync(FULL, ptx::mbar_wait(&red_full, flushes & 1, a.wait_limit, &abort_flag)))
                 return false;
             const int c0 = (u * a.ipu) / a.ipc;
             float* pp = a.part + ((size_t)u * a.max_slots + (blockIdx.x - c0)) * PW;
@@ -784,9 +786,14 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_kernel(const AttnArgs a) 
             return true;
         };
 
+        if (a.stall && w == 0 &&
+            !__all_sync(FULL, ptx::mbar_wait(&never, 0, a.wait_limit, &abort_flag))) {
+            give_up();
+            alive = false;
+        }
         for (int it = 0; it < nitems && alive; ++it) {
             const int st = it % ATT_STAGES;
-            if (!__all_sync(FULL, ptx::mbar_wait(&full[st], (it / ATT_STAGES) & 1, WAIT_LIMIT, &abort_flag))) {
+            if (!__all_sync(FULL, ptx::mbar_wait(&full[st], (it / ATT_STAGES) & 1, a.wait_limit, &abort_flag))) {
                 give_up();
                 alive = false;
                 break;
@@ -927,7 +934,7 @@ template <typename T, int G>
 cudaError_t launch_attn_t(const void* q, const void* K, const void* V, const int32_t* idx,
                           const int32_t* count, int units, int max_len, int sinks,
                           int clustered_end, int cur_len, int B, float* out, float* part,
-                          int32_t* counters, int max_splits, int32_t* dev_err, int num_sms,
+                          int max_splits, int32_t* dev_err, int num_sms, long long wait_limit, int stall,
                           cudaStream_t st) {
     using S = AttnShape<T, G>;
     AttnArgs a;
@@ -955,8 +962,9 @@ cudaError_t launch_attn_t(const void* q, const void* K, const void* V, const int
     a.qscale = 1.4426950408889634f / sqrtf((float)D);
     a.out = out;
     a.part = part;
-    a.counters = counters;
     a.dev_err = dev_err;
+    a.wait_limit = wait_limit;
+    a.stall = stall;
     auto kern = attn_kernel<T, G>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::SMEM);
     if (e != cudaSuccess) return e;
@@ -1047,11 +1055,11 @@ int attention_rows_per_split(int kv_dtype, int g) {
 cudaError_t launch_attention(const void* q, const void* K, const void* V, const int32_t* idx,
                              const int32_t* count, int units, int g, int kv_dtype, int max_len,
                              int sinks, int clustered_end, int cur_len, int B, float* out,
-                             float* part, int32_t* counters, int max_splits, int32_t* dev_err,
-                             int num_sms, cudaStream_t s) {
+                             float* part, int max_splits, int32_t* dev_err,
+                             int num_sms, long long wait_limit, int stall, cudaStream_t s) {
 #define CKV_ATTN(T, G)                                                                          \
     return launch_attn_t<T, G>(q, K, V, idx, count, units, max_len, sinks, clustered_end,      \
-                               cur_len, B, out, part, counters, max_splits, dev_err, num_sms, s)
+                               cur_len, B, out, part, max_splits, dev_err, num_sms, wait_limit, stall, s)
     if (kv_dtype == CKV_BF16) {
         // bf16 K/V: tensor-core kernel (attn_mma.cu); fp32 K/V: CUDA-core kernel below
         return launch_attention_mma(q, K, V, idx, count, units, g, max_len, sinks, clustered_end, cur_len, B,

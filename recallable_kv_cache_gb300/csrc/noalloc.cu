@@ -6,9 +6,11 @@
 // memory to a pooling allocator.  ckv_sparse_decode_attn needs a context, and
 // creating one allocates the split-K workspace.  This entry point runs the same
 // attention kernel without a context: its only scratch (the per-split partial
-// results and the per-unit arrival counters of the split combine) lives in one
-// fixed-size array in the library's own device memory, reserved when the
-// library is loaded and kept until the process exits.
+// results that the combine kernel merges) lives in one fixed-size array in the
+// library's own device memory, reserved when the library is loaded and kept
+// until the process exits.  The array's address is looked up once per device
+// in the device's primary context (the one the runtime API uses); a
+// cudaDeviceReset invalidates it.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -61,6 +63,7 @@ extern "C" ckv_status ckv_sparse_decode_attn_noalloc(const void* q, int32_t q_dt
                                                      int32_t max_len, int32_t sinks, int32_t clustered_end,
                                                      int32_t cur_len, int32_t B, float* out,
                                                      int32_t* dev_err, void* stream) {
+    CKV_TRACE("ckv_sparse_decode_attn_noalloc");
     using namespace ckv;
     if (!q || !K || !V || !idx || !count || !out) return CKV_ERR_ARG;
     if (q_dtype != CKV_F32 && q_dtype != CKV_BF16) return CKV_ERR_DTYPE;
@@ -73,20 +76,17 @@ extern "C" ckv_status ckv_sparse_decode_attn_noalloc(const void* q, int32_t q_dt
     const int rs = attention_rows_per_split(q_dtype, g);
     const long long rows = (long long)sinks + (cur_len - clustered_end) + B;
     const long long splits = (rows + rs - 1) / rs;
-    const long long part_bytes = (long long)units * splits * g * (D + 2) * (long long)sizeof(float);
-    const long long cnt_off = (part_bytes + 255) / 256 * 256;
-    const long long need = cnt_off + (long long)units * (long long)sizeof(int32_t);
+    const long long need = (long long)units * splits * g * (D + 2) * (long long)sizeof(float);
     if (need > (long long)SCRATCH_BYTES) return CKV_ERR_CAPACITY;
 
     void* base = nullptr;
     int num_sms = 0;
     if (scratch_address(&base, &num_sms) != cudaSuccess) return CKV_ERR_CUDA;
+    // every partial the combine reads is written by the same call first: what
+    // the previous call left in the array is never read
     float* part = static_cast<float*>(base);
-    int32_t* counters = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(base) + cnt_off);
     cudaStream_t s = (cudaStream_t)stream;
-    // the split combine counts arrivals from zero; the previous call's contents remain
-    if (cudaMemsetAsync(counters, 0, (size_t)units * sizeof(int32_t), s) != cudaSuccess) return CKV_ERR_CUDA;
     const cudaError_t e = launch_attention(q, K, V, idx, count, units, g, q_dtype, max_len, sinks, clustered_end,
-                                           cur_len, B, out, part, counters, (int)splits, dev_err, num_sms, s);
+                                           cur_len, B, out, part, (int)splits, dev_err, num_sms, WAIT_LIMIT, 0, s);
     return e == cudaSuccess ? CKV_OK : CKV_ERR_CUDA;
 }

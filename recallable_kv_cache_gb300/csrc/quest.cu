@@ -121,6 +121,7 @@ using namespace ckv;
 
 extern "C" ckv_status ckv_quest_pages(const void* K, int32_t kv_dtype, int32_t units, int32_t max_len, int32_t sinks,
                                       int32_t L, void* page_max, void* page_min, void* stream) {
+    CKV_TRACE("ckv_quest_pages");
     if (!K || !page_max || !page_min) return CKV_ERR_ARG;
     if (kv_dtype != CKV_F32 && kv_dtype != CKV_BF16) return CKV_ERR_DTYPE;
     if (units < 1 || sinks < 0 || L <= sinks || L > max_len) return CKV_ERR_ARG;
@@ -140,6 +141,7 @@ extern "C" ckv_status ckv_quest_pages(const void* K, int32_t kv_dtype, int32_t u
 
 extern "C" ckv_status ckv_quest_score(const void* q, int32_t q_dtype, const void* page_max, const void* page_min,
                                       int32_t units, int32_t g, int32_t n_pages, float* scores, void* stream) {
+    CKV_TRACE("ckv_quest_score");
     if (!q || !page_max || !page_min || !scores) return CKV_ERR_ARG;
     if (q_dtype != CKV_F32 && q_dtype != CKV_BF16) return CKV_ERR_DTYPE;
     if (units < 1 || n_pages < 1) return CKV_ERR_ARG;

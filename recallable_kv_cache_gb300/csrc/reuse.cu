@@ -72,6 +72,7 @@ using namespace ckv;
 extern "C" ckv_status ckv_selection_overlap(int32_t units, int32_t max_len, int32_t R, const int32_t* const* idx_prev,
                                             const int32_t* const* cnt_prev, int32_t B_prev, const int32_t* idx_cur,
                                             const int32_t* cnt_cur, int32_t B_cur, int32_t* hits, void* stream) {
+    CKV_TRACE("ckv_selection_overlap");
     if (units < 1 || max_len < 1 || R < 0 || R > REUSE_MAX_R || B_prev < 0 || B_cur < 0) return CKV_ERR_ARG;
     if (!idx_cur || !cnt_cur || !hits || (R > 0 && (!idx_prev || !cnt_prev))) return CKV_ERR_ARG;
     PrevSets ps = {};

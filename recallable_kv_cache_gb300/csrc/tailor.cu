@@ -124,6 +124,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 using namespace ckv;
 
 extern "C" ckv_status ckv_centroid_channels(ckv_ctx* ctx, void* muT, float* chmax, void* stream) {
+    CKV_TRACE("ckv_centroid_channels");
     if (!ctx || !muT || !chmax) return CKV_ERR_ARG;
     if (!aligned16(muT) || !aligned16(chmax)) return CKV_ERR_ALIGN;
     if (ctx->n_clusters <= 0) return CKV_ERR_STATE;
@@ -143,6 +144,7 @@ extern "C" ckv_status ckv_centroid_channels(ckv_ctx* ctx, void* muT, float* chma
 extern "C" ckv_status ckv_channel_prescore(ckv_ctx* ctx, const void* q, int32_t q_dtype, const void* muT,
                                            const float* chmax, int32_t r, float* scores, int32_t* channels,
                                            void* stream) {
+    CKV_TRACE("ckv_channel_prescore");
     if (!ctx || !q || !muT || !chmax || !scores) return CKV_ERR_ARG;
     if (q_dtype != ctx->cfg.kv_dtype) return CKV_ERR_DTYPE;
     if (r < 1 || r > MAX_PRESCORE_R) return CKV_ERR_ARG;

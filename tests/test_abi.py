@@ -87,3 +87,7 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(ckv, "_LIB", None)
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         ckv.lib()
+
+
+def test_set_wait_limit_rejects_on_host(lib):
+    assert lib.ckv_set_wait_limit(None, 1000, 0) == -1

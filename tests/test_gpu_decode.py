@@ -252,3 +252,61 @@ def test_decode_step_equals_select_then_attention(case):
             toks = ck.attention_tokens(16, w.L, cur_len, idx[u, :cnt[u]])
             want = ck.sparse_attention(to64(case["Q"][qi][u]), to64(case["K"][u]), to64(case["V"][u]), toks)
             assert np.abs(got[u] - want).max() <= ATTN_TOL[w.dtype]
+
+
+@pytest.mark.parametrize("C", [13, 129, 409, 1000])
+def test_decode_step_selection_edge_cases(C):
+    """ckv_decode_step selects inside its attention kernel (one warp per unit,
+    a size-weighted radix select over the score bits, then a sort of the
+    clusters that can be taken).  Against the oracle, given the GPU's own
+    scores: random cluster layouts with empty clusters, duplicated centroids
+    (tied scores), a zero query (every score tied: rank by cluster index),
+    budgets 0, 1, ragged, at and above the clustered tokens; the attention
+    over the selection against the oracle."""
+    torch.cuda.init()
+    U, g, d, pend = 3, 4, 128, 21
+    rng = np.random.default_rng(1000 + C)
+    n = 7 * C + 5
+    L = 16 + n
+    max_len = L + 64
+    ctx = make_ctx(U, g, max_len, C, n + 50, "bf16")
+    states = []
+    for u in range(U):
+        labels = rng.integers(0, C, size=n)
+        labels[labels % 5 == 2] = C - 1          # some clusters stay empty, one grows
+        sizes, offsets, perm = ck.build_csr(labels, C, 16)
+        mu = rng.standard_normal((C, d))
+        mu[1::4] = mu[0]                         # duplicated rows: tied scores
+        mu = torch.from_numpy(mu).to(torch.bfloat16).double().numpy()   # exact in the bf16 copy
+        states.append(dict(mu=mu, sizes=sizes, offsets=offsets, perm=perm))
+    upload_state(ctx, states, L)
+    K = torch.from_numpy(rng.standard_normal((U, max_len, d))).to(torch.bfloat16)
+    V = torch.from_numpy(rng.standard_normal((U, max_len, d))).to(torch.bfloat16)
+    Kd, Vd = K.cuda().contiguous(), V.cuda().contiguous()
+    cur_len = L + pend
+    qs = [torch.from_numpy(rng.standard_normal((U, g, d))).to(torch.bfloat16), torch.zeros(U, g, d, dtype=torch.bfloat16)]
+    for q in qs:
+        qd = q.cuda().contiguous()
+        sc = torch.empty(U, C, dtype=torch.float32, device="cuda")
+        ctx.score(qd, sc)
+        for B in sorted({b for b in (0, 1, 57, 700, n, n + 50) if b <= n + 50}):
+            i1 = torch.full((U, max(B, 1)), -5, dtype=torch.int32, device="cuda")
+            c1 = torch.empty(U, dtype=torch.int32, device="cuda")
+            o1 = torch.empty(U, g, d, dtype=torch.float32, device="cuda")
+            ctx.decode_step(qd, Kd, Vd, B, cur_len, i1, c1, o1)
+            i2, c2 = torch.full_like(i1, -5), torch.empty_like(c1)
+            ctx.select(qd, B, i2, c2)
+            torch.cuda.synchronize()
+            assert ctx.device_error() == 0
+            assert torch.equal(c1, c2) and torch.equal(i1, i2)
+            scores, idx, cnt, out = sc.cpu().numpy(), i1.cpu().numpy(), c1.cpu().numpy(), to64(o1)
+            for u in range(U):
+                st = states[u]
+                want, wc = ck.select(scores[u].astype(np.float64), st["sizes"], st["offsets"], st["perm"], B)
+                assert cnt[u] == wc == min(B, n)
+                assert np.array_equal(idx[u, :wc], want)
+                assert (idx[u, wc:] == -5).all()
+                toks = ck.attention_tokens(16, L, cur_len, idx[u, :wc])
+                ref = ck.sparse_attention(to64(q[u]), to64(K[u]), to64(V[u]), toks)
+                assert np.abs(out[u] - ref).max() <= ATTN_TOL["bf16"]
+    ctx.close()

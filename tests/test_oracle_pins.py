@@ -16,6 +16,7 @@ import pytest
 import torch
 
 import oracle.clusterkv as ck
+import oracle.cpp as cc
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -389,6 +390,13 @@ PINS = [pin_selection_worked_example, pin_cluster_count, pin_bf16_rounding,
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
 def test_oracle_pin(pin):
     pin(ck)
+
+
+# the same pins against the C++ oracle (the recall helpers are measurement
+# code of the numpy oracle only)
+@pytest.mark.parametrize("pin", [p for p in PINS if p is not pin_recall_properties], ids=lambda f: f.__name__)
+def test_cpp_oracle_pin(pin):
+    pin(cc)
 
 
 # ----------------------------------------------------------------------------

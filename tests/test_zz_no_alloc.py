@@ -14,14 +14,18 @@ from recallable_kv_cache_gb300 import ckv, synth
 pytestmark = pytest.mark.gpu
 
 
-def test_noalloc_matches_context_entry_point_twice():
+@pytest.mark.parametrize("dtype,g", [("bf16", 4), ("f32", 1), ("f32", 8)])
+def test_noalloc_matches_context_entry_point_twice(dtype, g):
+    """bf16 K/V (tensor-core kernel, 16-row work items) and fp32 K/V with one and
+    eight query heads per KV head (the fp32 kernel's work items hold 64 and 32
+    rows, which sets the split count the scratch must hold)."""
     torch.cuda.init()
-    w = synth.scaled(synth.WORKLOADS["layer_32k"], units=3, L=16 + 1200, decode_steps=60, C=15,
-                     n_centres=15, B=256)
+    base = synth.WORKLOADS["layer_32k" if dtype == "bf16" else "tiny_2k"]
+    w = synth.scaled(base, units=3, g=g, L=16 + 1200, decode_steps=60, C=15, n_centres=15, B=256)
     K, V = synth.make_kv(w)
     Q = synth.make_queries(w, 2)
     states = [ck.cluster_prefill(to64(K[u]), w.L, w.C, iters=2) for u in range(w.units)]
-    ctx = make_ctx(w.units, w.g, w.max_len, w.C, w.B, "bf16")
+    ctx = make_ctx(w.units, w.g, w.max_len, w.C, w.B, w.dtype)
     upload_state(ctx, states, w.L)
     Kd, Vd = K.cuda().contiguous(), V.cuda().contiguous()
     idx = torch.empty(w.units, w.B, dtype=torch.int32, device="cuda")
@@ -38,7 +42,7 @@ def test_noalloc_matches_context_entry_point_twice():
                                        got, dev_err=err)
         torch.cuda.synchronize()
         diff = (got - want).abs().max().item()
-        assert diff <= ATTN_TOL["bf16"], (call, diff)
+        assert diff <= ATTN_TOL[w.dtype], (call, diff)
         assert int(err.item()) == 0
     ctx.close()
 
