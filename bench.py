@@ -53,6 +53,7 @@ def parse():
     p.add_argument("--workload", default=WORKLOAD)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-workloads", action="store_true", help="skip the other workloads' measurements")
     p.add_argument("--no-comparators", action="store_true", help="skip the Quest / reuse / channel / full-KV side "
                                                                   "measurements")
     p.add_argument("--units", type=int, default=0, help="override the unit count (small profiling cases)")
@@ -174,19 +175,22 @@ class ExternalEvents:
 
 
 # ----------------------------------------------------------------------------- algorithmic bytes
-def decode_bytes(w, step: int, C: int, async_incr: bool = False):
+def decode_bytes(w, step: int, C: int, async_incr: bool = False, pend: int | None = None):
     """Algorithmic HBM bytes of decode step `step` for all units: (attention, whole step).
-    Attention reads every attended K and V row once (bf16, 256 B each) for all
-    g heads, the indices, q, and writes out (fp32).  Scoring reads the bf16
-    centroid table and q, writes the scores; selection reads scores, sizes,
-    offsets and the selected perm entries, writes idx and count."""
+    Attention reads every attended K and V row once (256 B each in bf16, 512
+    in fp32) for all g heads, the indices, q, and writes out (fp32).  Scoring
+    reads the centroid scoring copy and q, writes the scores; selection reads
+    scores, sizes, offsets and the selected perm entries, writes idx and
+    count.  `pend` overrides the pending tokens of the step."""
     U, g, d, B = w.units, w.g, w.d, w.B
-    pend = step % w.m + 1
-    if async_incr and step >= w.m and step % w.m == 0:
-        pend += w.m  # the block being clustered on the side stream is still pending
+    e = 4 if w.dtype == "f32" else 2
+    if pend is None:
+        pend = step % w.m + 1
+        if async_incr and step >= w.m and step % w.m == 0:
+            pend += w.m  # the block being clustered on the side stream is still pending
     rows = w.sinks + pend + B
-    attn = U * (rows * 2 * d * 2 + B * 4 + 4 + g * d * 2 + g * d * 4)
-    score = U * (C * d * 2 + g * d * 2 + C * 4)
+    attn = U * (rows * 2 * d * e + B * 4 + 4 + g * d * e + g * d * 4)
+    score = U * (C * d * e + g * d * e + C * 4)
     select = U * (C * 4 + C * 4 + (C + 1) * 4 + B * 4 + B * 4 + 4)
     return attn, attn + score + select
 
@@ -832,6 +836,99 @@ def run_e2e(ctx, w, K, V, Q, one_call=False, sync_incremental=False):
             "step_io": "zero-copy (kernels access pinned host memory)" if zero_copy else "copy nodes"}
 
 
+# ----------------------------------------------------------------------------- the other workloads
+OTHER_WORKLOADS = ("tiny_2k", "layer_32k", "batch16_32k", "long_128k")
+
+
+def measure_workload(name, hbm, reps=2):
+    """One workload of the survey's set on this GPU, beside the main line:
+    prefill clustering of every unit (CUDA events, after a warm-up run) and
+    K-means ms per layer; for the decode loops (batch16_32k, long_128k) the
+    whole decode loop of the job as one CUDA graph (append the step's K/V row,
+    selection, attention) and its roofline; for the single-step workloads
+    (tiny_2k: 8 independent queries of one fp32 head; layer_32k: one step of a
+    layer) the latency of a decode step.  Inputs generated on the device."""
+    from recallable_kv_cache_gb300 import ckv
+    w = synth.WORKLOADS[name]
+    U, L, B = w.units, w.L, w.B
+    T = max(w.decode_steps, 1)
+    K, V = synth.make_kv(w, device="cuda")
+    Q = synth.make_queries(w, w.n_queries if w.decode_steps == 0 else T, device="cuda")
+    ctx = ckv.Context(units=U, g=w.g, max_len=w.max_len, max_clusters=w.max_clusters, max_budget=B,
+                      kv_dtype=w.dtype, iters=w.iters, m=w.m, c_plus=w.c_plus)
+    s = torch.cuda.Stream()
+    e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    res = {"units": U, "L": L, "B": B, "C": w.C, "dtype": w.dtype}
+    with torch.cuda.stream(s):
+        ctx.cluster_prefill(K, L, w.C, stream=s)
+        ts = []
+        for _ in range(reps):
+            e0.record(s)
+            ctx.cluster_prefill(K, L, w.C, stream=s)
+            e1.record(s)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+    prefill_ms = statistics.mean(ts)
+    res["prefill_ms"] = prefill_ms
+    res["kmeans_ms_per_layer"] = prefill_ms * w.kv_heads * w.batch / U
+    kflops, _ = kmeans_flops_bytes(w)
+    res["kmeans_tflops"] = kflops / (prefill_ms / 1000.0) / 1e12
+    idx = torch.empty(U, B, dtype=torch.int32, device="cuda")
+    cnt = torch.empty(U, dtype=torch.int32, device="cuda")
+    out = torch.empty(U, w.g, w.d, dtype=torch.float32, device="cuda")
+    g = torch.cuda.CUDAGraph()
+    if w.decode_steps > 0:
+        Knew, Vnew = K[:, L:L + T].clone(), V[:, L:L + T].clone()
+
+        def body():
+            for t in range(T):
+                ckv.append_kv(Knew[:, t:t + 1], Vnew[:, t:t + 1], K, V, L + t, stream=s)
+                ctx.decode_step(Q[t], K, V, B, L + t + 1, idx, cnt, out, stream=s)
+        steps = T
+    else:
+        n_q = Q.shape[0]
+
+        def body():
+            for i in range(64):
+                ctx.decode_step(Q[i % n_q], K, V, B, L, idx, cnt, out, stream=s)
+        steps = 64
+    with torch.cuda.stream(s):
+        body()
+        with torch.cuda.graph(g, stream=s):
+            body()
+        g.replay()
+        ts = []
+        for _ in range(reps):
+            e1.record(s)
+            g.replay()
+            e2.record(s)
+            torch.cuda.synchronize()
+            ts.append(e1.elapsed_time(e2))
+    assert ctx.device_error() == 0
+    step_us = 1000.0 * statistics.mean(ts) / steps
+    byts = (statistics.mean(decode_bytes(w, t, w.C)[1] for t in range(T)) if w.decode_steps > 0
+            else decode_bytes(w, 0, w.C, pend=0)[1])
+    if w.decode_steps > 0:
+        byts += U * 2 * w.d * (4 if w.dtype == "f32" else 2) * 2  # the appended row, read and written
+        job_ms = prefill_ms + statistics.mean(ts)
+        res["tokens_per_s"] = w.batch * T / (job_ms / 1000.0)
+        res["decode_tokens_per_s"] = w.batch * T / (statistics.mean(ts) / 1000.0)
+        res["job_ms"] = job_ms
+        res["what"] = (f"whole job: prefill clustering + {T} decode steps (append + ckv_decode_step) as one graph; "
+                       "no incremental clustering in this workload")
+    else:
+        res["what"] = (f"one decode step (ckv_decode_step: scoring, selection, attention) over the prompt, "
+                       f"{w.n_queries} different queries cycled, 64 steps per graph replay")
+    gbs = byts / (step_us / 1e6) / 1e9
+    res["decode_step_us"] = step_us
+    res["decode_roofline"] = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                              "bytes_per_step": byts}
+    ctx.close()
+    del K, V, Q
+    torch.cuda.empty_cache()
+    return res
+
+
 # ----------------------------------------------------------------------------- the oracle on the CPU
 def oracle_jobs(w, n_units=None, device_tensors=None):
     """The C++ oracle (float64, oracle/clusterkv_ref.cpp) on whole jobs of the
@@ -1005,6 +1102,11 @@ def main():
                                 "sample": f"{n_units} units' whole jobs (prefill clustering + {T} decode steps each) "
                                           f"on {threads} threads in {cb['wall_s']:.1f} s, extrapolated "
                                           f"x{w.units}/{n_units} units"}
+    if rank == 0 and world == 1 and not args.no_workloads and args.workload == WORKLOAD:
+        # the main workload's tensors go first: the batch-16 and 128k jobs hold ~69 GB each
+        r.clear()
+        torch.cuda.empty_cache()
+        line["workloads"] = {n: measure_workload(n, hbm) for n in OTHER_WORKLOADS}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

@@ -363,12 +363,10 @@ ckv_status ckv_import_clusters(ckv_ctx* ctx, int32_t n_clusters, int32_t cluster
  * tensor-core operations it already started complete (each of those waits
  * bounded the same way), releases its tensor memory and returns; the context
  * stays usable.  ckv_set_wait_limit sets that limit for this context's later
- * launches (1 <= cycles <= 4e9).  stall = 1 makes the next launches of three
- * kernels wait once on something nothing ever completes, so that their
- * failure path runs: the tensor-core K-means assignment (bf16 keys), the fp32
- * sparse attention, and the one-kernel decode step of ckv_decode_step (whose
- * selections are then never published: its attention warps give up and treat
- * every selection as empty, and idx / count are not written).  stall = 0
+ * launches (1 <= cycles <= 4e9).  stall = 1 makes the next launches of two
+ * kernels wait once on a barrier nothing ever completes, so that their
+ * failure path runs: the tensor-core K-means assignment (bf16 keys) and the
+ * fp32 sparse attention (whose outputs are then not valid).  stall = 0
  * restores normal operation.  This exists to test failure detection (see
  * ckv_get_device_error) without faulting or hanging a GPU.
  * Errors: CKV_ERR_ARG. */

@@ -114,9 +114,19 @@ def _stream(stream):
     return getattr(stream, "cuda_stream", stream)
 
 
+def _is_tensor(t) -> bool:
+    return hasattr(t, "shape") and hasattr(t, "data_ptr")
+
+
 class Context:
     """One library context: the cluster state of `units` (sequence, layer, KV
-    head) triples, allocated on the current CUDA device."""
+    head) triples, allocated on the current CUDA device.
+
+    Tensor arguments are checked against the context's layout before the call
+    (the C ABI takes plain pointers and cannot see extents): K and V must be
+    contiguous [units, max_len, d], q contiguous [units, g, d], idx [units, >= B]
+    and count [units] int32, out [units, g, d]; a mismatch raises ValueError
+    and nothing is launched."""
 
     def __init__(self, units: int, g: int, max_len: int, max_clusters: int, max_budget: int,
                  kv_dtype: str = "bf16", d: int = 128, sinks: int = 16, ratio: int = 80,
@@ -126,6 +136,29 @@ class Context:
         h = ctypes.c_void_p()
         _check(lib().ckv_create(ctypes.byref(self.cfg), ctypes.byref(h)), "ckv_create")
         self.handle = h
+
+    def _kv(self, *ts):
+        for t in ts:
+            if _is_tensor(t) and (tuple(t.shape) != (self.cfg.units, self.cfg.max_len, self.cfg.d)
+                                  or not t.is_contiguous()):
+                raise ValueError(f"K/V must be contiguous [{self.cfg.units}, {self.cfg.max_len}, {self.cfg.d}], "
+                                 f"got {tuple(t.shape)}")
+
+    def _q(self, q):
+        if _is_tensor(q) and (tuple(q.shape) != (self.cfg.units, self.cfg.g, self.cfg.d) or not q.is_contiguous()):
+            raise ValueError(f"q must be contiguous [{self.cfg.units}, {self.cfg.g}, {self.cfg.d}], got {tuple(q.shape)}")
+
+    def _sel(self, B, idx, count):
+        if _is_tensor(idx) and (idx.dim() != 2 or idx.shape[0] != self.cfg.units or idx.shape[1] < max(B, 1)
+                                or not idx.is_contiguous() or idx.stride(0) != B and B > 0):
+            raise ValueError(f"idx must be contiguous [{self.cfg.units}, B={B}], got {tuple(idx.shape)}")
+        if _is_tensor(count) and tuple(count.shape) != (self.cfg.units,):
+            raise ValueError(f"count must be [{self.cfg.units}], got {tuple(count.shape)}")
+
+    def _out(self, out):
+        if _is_tensor(out) and (tuple(out.shape) != (self.cfg.units, self.cfg.g, self.cfg.d) or not out.is_contiguous()):
+            raise ValueError(f"out must be contiguous [{self.cfg.units}, {self.cfg.g}, {self.cfg.d}], "
+                             f"got {tuple(out.shape)}")
 
     def close(self):
         if getattr(self, "handle", None):
@@ -146,6 +179,7 @@ class Context:
 
     # -- clustering ------------------------------------------------------------
     def cluster_prefill(self, K, L: int, n_clusters: int = 0, stream=None):
+        self._kv(K)
         _check(lib().ckv_cluster_prefill(self.handle, ptr(K), L, n_clusters, _stream(stream)),
                "ckv_cluster_prefill")
 
@@ -153,6 +187,7 @@ class Context:
                             stream=None):
         m = self.cfg.m if m is None else m
         c_plus = self.cfg.c_plus if c_plus is None else c_plus
+        self._kv(K)
         _check(lib().ckv_cluster_incremental(self.handle, ptr(K), start, m, c_plus, _stream(stream)),
                "ckv_cluster_incremental")
 
@@ -160,6 +195,7 @@ class Context:
                                   stream=None):
         m = self.cfg.m if m is None else m
         c_plus = self.cfg.c_plus if c_plus is None else c_plus
+        self._kv(K)
         _check(lib().ckv_cluster_incremental_begin(self.handle, ptr(K), start, m, c_plus, _stream(stream)),
                "ckv_cluster_incremental_begin")
 
@@ -168,15 +204,18 @@ class Context:
                "ckv_cluster_incremental_commit")
 
     def kmeans_assign(self, K, L: int, labels, stream=None):
+        self._kv(K)
         _check(lib().ckv_kmeans_assign(self.handle, ptr(K), L, ptr(labels), _stream(stream)),
                "ckv_kmeans_assign")
 
     def kmeans_update(self, K, L: int, labels, stream=None):
+        self._kv(K)
         _check(lib().ckv_kmeans_update(self.handle, ptr(K), L, ptr(labels), _stream(stream)),
                "ckv_kmeans_update")
 
     # -- decode ----------------------------------------------------------------
     def score(self, q, scores, stream=None):
+        self._q(q)
         _check(lib().ckv_score(self.handle, ptr(q), _dtype_code(q), ptr(scores), _stream(stream)),
                "ckv_score")
 
@@ -195,15 +234,25 @@ class Context:
                                        _stream(stream)), "ckv_select_scored")
 
     def select(self, q, B: int, idx, count, stream=None):
+        self._q(q)
+        self._sel(B, idx, count)
         _check(lib().ckv_select(self.handle, ptr(q), _dtype_code(q), B, ptr(idx), ptr(count),
                                 _stream(stream)), "ckv_select")
 
     def sparse_decode_attn(self, q, K, V, idx, count, B: int, cur_len: int, out, stream=None):
+        self._q(q)
+        self._kv(K, V)
+        self._sel(B, idx, count)
+        self._out(out)
         _check(lib().ckv_sparse_decode_attn(self.handle, ptr(q), _dtype_code(q), ptr(K), ptr(V),
                                             ptr(idx), ptr(count), B, cur_len, ptr(out),
                                             _stream(stream)), "ckv_sparse_decode_attn")
 
     def decode_step(self, q, K, V, B: int, cur_len: int, idx, count, out, stream=None):
+        self._q(q)
+        self._kv(K, V)
+        self._sel(B, idx, count)
+        self._out(out)
         _check(lib().ckv_decode_step(self.handle, ptr(q), _dtype_code(q), ptr(K), ptr(V), B, cur_len, ptr(idx),
                                      ptr(count), ptr(out), _stream(stream)), "ckv_decode_step")
 

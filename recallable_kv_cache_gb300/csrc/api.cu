@@ -34,8 +34,7 @@ cudaError_t alloc(T** p, size_t count) {
 void free_all(ckv_ctx* c) {
     void* ptrs[] = {c->mu32,   c->mu_s == c->mu32 ? nullptr : c->mu_s, c->mu_hat, c->sizes,
                     c->offsets, c->perm, c->labels, c->chunk_cnt, c->task_off, c->task_cl,
-                    c->seg_part, c->scores, c->attn_part, c->dev_err, c->assign_best,
-                    c->sel_flag};
+                    c->seg_part, c->scores, c->attn_part, c->dev_err, c->assign_best};
     for (void* p : ptrs)
         if (p) cudaFree(p);
     if (c->pend_done) cudaEventDestroy(c->pend_done);
@@ -105,10 +104,8 @@ ckv_status ckv_create(const ckv_config* cfg, ckv_ctx** out) {
     c->max_tasks = ceil_div(c->ntok, SEG_ROWS) + c->cmax;
     c->attn_rows = cfg->sinks + cfg->max_budget + 2 * cfg->m;
     c->max_splits = ceil_div(c->attn_rows, attention_rows_per_split(cfg->kv_dtype, cfg->g));
-    if (c->max_splits < STEP_MIN_SLOTS) c->max_splits = STEP_MIN_SLOTS;
     c->wait_limit = WAIT_LIMIT;
     c->stall = 0;
-    c->sel_flag_dirty = false;
     c->elem = cfg->kv_dtype == CKV_BF16 ? 2 : 4;
     c->last_stream = nullptr;
     c->pend_m = 0;
@@ -135,7 +132,6 @@ ckv_status ckv_create(const ckv_config* cfg, ckv_ctx** out) {
     ok = ok && alloc(&c->scores, U * c->cmax) == cudaSuccess;
     ok = ok && alloc(&c->attn_part, U * c->max_splits * cfg->g * (D + 2)) == cudaSuccess;
     ok = ok && alloc(&c->dev_err, 1) == cudaSuccess;
-    ok = ok && alloc(&c->sel_flag, U) == cudaSuccess;
     ok = ok && cudaEventCreateWithFlags(&c->pend_done, cudaEventDisableTiming) == cudaSuccess;
     if (cfg->kv_dtype == CKV_BF16 && c->cmax_pad > MAX_ASSIGN_CPAD)
         ok = ok && alloc(&c->assign_best, U * c->ntok) == cudaSuccess;
@@ -143,7 +139,6 @@ ckv_status ckv_create(const ckv_config* cfg, ckv_ctx** out) {
         const size_t hat = U * (size_t)c->cmax_pad * D * c->elem;
         ok = cudaMemset(c->mu_hat, 0, hat) == cudaSuccess &&
              cudaMemset(c->dev_err, 0, 4) == cudaSuccess && cudaMemset(c->sizes, 0, U * c->cmax * 4) == cudaSuccess &&
-             cudaMemset(c->sel_flag, 0, U * 4) == cudaSuccess &&
              cudaDeviceSynchronize() == cudaSuccess;
     }
     if (!ok) {
@@ -357,20 +352,6 @@ ckv_status ckv_decode_step(ckv_ctx* ctx, const void* q, int32_t q_dtype, const v
     if (ctx->n_clusters > MAX_SELECT_CLUSTERS) return CKV_ERR_UNIMPLEMENTED;
     cudaStream_t s = (cudaStream_t)stream;
     ctx->last_stream = s;
-    if (step_supported(ctx->cfg.kv_dtype, ctx->cfg.g, ctx->n_clusters, ctx->cfg.units, ctx->num_sms)) {
-        // scoring, then one kernel that selects and attends (its attention warps
-        // stream the sinks and pending rows while its selector warps rank the
-        // clusters), then the combine
-        cudaError_t e = cudaSuccess;
-        if (ctx->sel_flag_dirty) e = cudaMemsetAsync(ctx->sel_flag, 0, (size_t)ctx->cfg.units * 4, s);
-        if (e == cudaSuccess) e = launch_score(ctx, q, ctx->n_clusters, ctx->scores, ctx->cmax, s, true);
-        if (e == cudaSuccess) {
-            ctx->sel_flag_dirty = false;
-            e = launch_step(ctx, q, K, V, ctx->n_clusters, B, cur_len, idx, count, out, ctx->wait_limit, s);
-            if (e != cudaSuccess) ctx->sel_flag_dirty = true;
-        }
-        return cuda_status(e);
-    }
     // selection, then attention (a dependent launch: it is scheduled while the
     // selection drains and waits for it on the device)
     cudaError_t e = launch_select(ctx, q, nullptr, 0, ctx->n_clusters, B, idx, count, s);

@@ -26,8 +26,6 @@ constexpr int MAX_ASSIGN_CPAD = 640;  // centroid rows the assignment keeps resi
 constexpr long long WAIT_LIMIT = 2000000000LL;  // SM cycles before a bounded wait gives up (default)
 constexpr long long MAX_WAIT_LIMIT = 4000000000LL;  // largest limit ckv_set_wait_limit accepts
 constexpr int QUEST_PAGE = 16;     // tokens per page of the page-granular comparator
-constexpr int STEP_MAX_CLUSTERS = 1024;  // clusters per unit the one-kernel decode step selects from
-constexpr int STEP_MIN_SLOTS = 20;       // partial slots per unit the one-kernel decode step may use
 
 inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
@@ -91,8 +89,6 @@ struct ckv_ctx {
     float* attn_part;   // [U][max_splits][g * (D + 2)]
     int32_t* dev_err;   // device error word
     float* assign_best; // [U][ntok] running arg-max values between assignment passes (large C only)
-    int32_t* sel_flag;  // [U] selection-ready flags of the one-kernel decode step (0 between steps)
-    bool sel_flag_dirty; // a step kernel ran without its combine: clear the flags first
     long long wait_limit; // SM cycles before a bounded device wait gives up
     int stall;            // failure detection test: kernels first wait on something nothing completes
 };
@@ -131,12 +127,6 @@ cudaError_t launch_attention(const void* q, const void* K, const void* V, const 
 // are bounded by ceil(rows / this))
 int attention_rows_per_split(int kv_dtype, int g);
 int attention_mma_rows_per_tile();
-// one-kernel decode step (selection + attention; step.cu): whether it applies,
-// and the launch of the selection/attention kernel and its combine (the
-// scores must already be in ctx->scores)
-bool step_supported(int kv_dtype, int g, int C, int units, int num_sms);
-cudaError_t launch_step(const ckv_ctx* ctx, const void* q, const void* K, const void* V, int C, int B, int cur_len,
-                        int32_t* idx, int32_t* count, float* out, long long wait_limit, cudaStream_t s);
 cudaError_t launch_attention_mma(const void* q, const void* K, const void* V, const int32_t* idx,
                                  const int32_t* count, int units, int g, int max_len, int sinks, int clustered_end,
                                  int cur_len, int B, float* out, float* part, int max_slots, int32_t* dev_err,

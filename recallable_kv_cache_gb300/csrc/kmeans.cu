@@ -275,39 +275,56 @@ __global__ void __launch_bounds__(1024) csr_scan_kernel(int n, int C, int cmax, 
     (void)n;
 }
 
-__global__ void __launch_bounds__(1024) csr_scatter_kernel(const int32_t* __restrict__ labels, int n, int C,
-                                                           int cmax, int nchunk,
-                                                           const int32_t* __restrict__ chunk_cnt,
-                                                           const int32_t* __restrict__ offsets,
-                                                           int32_t* __restrict__ perm, int ntok, int sinks) {
-    extern __shared__ uint16_t wh[];  // [32 warps][C]
-    const int u = blockIdx.y, k = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    for (int e = tid; e < 32 * C; e += 1024) wh[e] = 0;
-    __syncthreads();
-    const int i = k * CSR_CHUNK + tid;
-    const bool valid = i < n;
-    int l = -1;
-    if (valid) {
-        l = labels[(size_t)u * n + i];
-        if (l < 0 || l >= C) l = 0;
-    }
-    const unsigned peers = __match_any_sync(FULL, l);
-    const int rank = __popc(peers & ((1u << lane) - 1u));
-    if (valid && rank == 0) wh[warp * C + l] = (uint16_t)__popc(peers);
-    __syncthreads();
-    for (int c = tid; c < C; c += 1024) {
-        int run = 0;
-        for (int w = 0; w < 32; ++w) {
-            const int v = wh[w * C + c];
-            wh[w * C + c] = (uint16_t)run;
-            run += v;
+// One warp per chunk of CSR_CHUNK tokens: a per-cluster cursor in shared
+// memory starts at the chunk's first position in each cluster's segment
+// (cluster offset + the earlier chunks' counts), then the chunk's tokens go by
+// in 32-token rounds, in index order: lanes with the same label find each other
+// (match_any), take consecutive positions by lane order from the cursor, and
+// the lowest of them advances it.  Every token lands at its stable
+// (label, index) position with no atomics.
+constexpr int SCATTER_WARPS = 8;
+
+__global__ void __launch_bounds__(32 * SCATTER_WARPS) csr_scatter_kernel(
+    const int32_t* __restrict__ labels, int n, int C, int cmax, int nchunk, const int32_t* __restrict__ chunk_cnt,
+    const int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int ntok, int sinks, int cstride) {
+    extern __shared__ int32_t cursor_all[];  // [SCATTER_WARPS][cstride]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int u = blockIdx.y, k = blockIdx.x * SCATTER_WARPS + warp;
+    if (k >= nchunk) return;
+    int32_t* cursor = cursor_all + warp * cstride;
+    const int32_t* cc = chunk_cnt + ((size_t)u * nchunk + k) * cmax;
+    const int32_t* of = offsets + (size_t)u * (cmax + 1);
+    for (int c = lane; c < C; c += 32) cursor[c] = of[c] + cc[c];
+    __syncwarp();
+    const int32_t* lab = labels + (size_t)u * n;
+    int32_t* pu = perm + (size_t)u * ntok;
+    const int i0 = k * CSR_CHUNK;
+    constexpr int ROUNDS = CSR_CHUNK / 32;
+    constexpr int PF = 8;  // label loads in flight per lane
+    for (int r0 = 0; r0 < ROUNDS; r0 += PF) {
+        int lv[PF];
+#pragma unroll
+        for (int j = 0; j < PF; ++j) {
+            const int i = i0 + 32 * (r0 + j) + lane;
+            int l = i < n ? lab[i] : -1;
+            if (i < n && (l < 0 || l >= C)) l = 0;  // reported by the count pass
+            lv[j] = l;
         }
-    }
-    __syncthreads();
-    if (valid) {
-        const int pos = offsets[(size_t)u * (cmax + 1) + l] + chunk_cnt[((size_t)u * nchunk + k) * cmax + l] +
-                        wh[warp * C + l] + rank;
-        perm[(size_t)u * ntok + pos] = sinks + i;
+#pragma unroll
+        for (int j = 0; j < PF; ++j) {
+            const int i = i0 + 32 * (r0 + j) + lane;
+            const int l = lv[j];
+            const unsigned peers = __match_any_sync(FULL, l);
+            const int leader = __ffs(peers) - 1;
+            int base = 0;
+            if (lane == leader && l >= 0) {
+                base = cursor[l];
+                cursor[l] = base + __popc(peers);
+            }
+            base = __shfl_sync(FULL, base, leader);
+            if (l >= 0) pu[base + __popc(peers & ((1u << lane) - 1u))] = sinks + i;
+            __syncwarp();
+        }
     }
 }
 
@@ -662,11 +679,12 @@ cudaError_t update_t(const ckv_ctx* ctx, const T* K, int n, int C, const int32_t
     csr_scan_kernel<<<U, 1024, ssm, s>>>(n, C, ctx->cmax, nchunk, ctx->chunk_cnt, ctx->sizes, ctx->offsets,
                                          ctx->task_off, ctx->task_cl, ctx->max_tasks);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const size_t wsm = (size_t)32 * C * sizeof(uint16_t);
+    const int cstride = round_up(C, 32);
+    const size_t wsm = (size_t)SCATTER_WARPS * cstride * sizeof(int32_t);
     e = cudaFuncSetAttribute(csr_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wsm);
     if (e != cudaSuccess) return e;
-    csr_scatter_kernel<<<dim3(nchunk, U), 1024, wsm, s>>>(labels, n, C, ctx->cmax, nchunk, ctx->chunk_cnt,
-                                                          ctx->offsets, ctx->perm, ctx->ntok, ctx->cfg.sinks);
+    csr_scatter_kernel<<<dim3(ceil_div(nchunk, SCATTER_WARPS), U), 32 * SCATTER_WARPS, wsm, s>>>(
+        labels, n, C, ctx->cmax, nchunk, ctx->chunk_cnt, ctx->offsets, ctx->perm, ctx->ntok, ctx->cfg.sinks, cstride);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int max_t = ceil_div(n, SEG_ROWS) + C;
     segsum_kernel<T><<<dim3(ceil_div(max_t, 8), U), 256, 0, s>>>(

@@ -86,26 +86,3 @@ def test_fp32_attention_wait_runs_out_then_recovers():
     assert ctx.device_error() == 0
     _check_attention(w, K, V, q, states, idx.cpu().numpy(), cnt.cpu().numpy(), to64(out), cur_len)
     ctx.close()
-
-
-def test_decode_step_flag_wait_runs_out_then_recovers():
-    """The one-kernel decode step: with no selection ever published, every
-    attention warp's wait on a unit's flag runs out (the selection counts as
-    empty); the flags are cleared by the step's combine, and the next step on
-    the context is correct."""
-    torch.cuda.init()
-    w, K, V, q, states, ctx = _decode_case("bf16", 4)
-    qd, Kd, Vd = q.cuda().contiguous(), K.cuda().contiguous(), V.cuda().contiguous()
-    idx = torch.empty(w.units, w.B, dtype=torch.int32, device="cuda")
-    cnt = torch.empty(w.units, dtype=torch.int32, device="cuda")
-    out = torch.empty(w.units, w.g, 128, dtype=torch.float32, device="cuda")
-    cur_len = w.L + 9
-    ctx.set_wait_limit(SHORT, stall=True)
-    ctx.decode_step(qd, Kd, Vd, w.B, cur_len, idx, cnt, out)
-    assert ctx.device_error() == TIMEOUT
-    ctx.set_wait_limit()
-    for _ in range(2):
-        ctx.decode_step(qd, Kd, Vd, w.B, cur_len, idx, cnt, out)
-        assert ctx.device_error() == 0
-        _check_attention(w, K, V, q, states, idx.cpu().numpy(), cnt.cpu().numpy(), to64(out), cur_len)
-    ctx.close()
