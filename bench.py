@@ -210,6 +210,42 @@ def kmeans_flops_bytes(w):
 
 
 # ----------------------------------------------------------------------------- our path
+class DecodeStep:
+    """Issues one decode step of every unit through the public calls on
+    stream `s`: the step's new K/V row into the caches, then either
+    ckv_decode_step (after the append) or ckv_select + ckv_sparse_decode_attn
+    with the append forked onto a side stream: the row is read only by the
+    attention, so the append overlaps the scoring and selection and is joined
+    before the attention (as a serving loop writes the new token's K/V while
+    the query is scored)."""
+
+    def __init__(self, ctx, K, V, B, idx, cnt, out, one_call, s):
+        self.ctx, self.K, self.V, self.B = ctx, K, V, B
+        self.idx, self.cnt, self.out = idx, cnt, out
+        self.one_call, self.s = one_call, s
+        self.side = torch.cuda.Stream()
+        self.fork, self.join = torch.cuda.Event(), torch.cuda.Event()
+
+    def __call__(self, q, k_row, v_row, pos, cur_len, before_decode=None):
+        from recallable_kv_cache_gb300 import ckv
+        s = self.s
+        if self.one_call:
+            ckv.append_kv(k_row, v_row, self.K, self.V, pos, stream=s)
+            if before_decode:
+                before_decode()
+            self.ctx.decode_step(q, self.K, self.V, self.B, cur_len, self.idx, self.cnt, self.out, stream=s)
+            return
+        self.fork.record(s)
+        self.side.wait_event(self.fork)
+        ckv.append_kv(k_row, v_row, self.K, self.V, pos, stream=self.side)
+        self.join.record(self.side)
+        if before_decode:
+            before_decode()
+        self.ctx.select(q, self.B, self.idx, self.cnt, stream=s)
+        s.wait_event(self.join)
+        self.ctx.sparse_decode_attn(q, self.K, self.V, self.idx, self.cnt, self.B, cur_len, self.out, stream=s)
+
+
 def rank_workload(w, rank: int, world: int):
     """Weak scaling: every rank runs the whole workload on its own units (its
     own sequences: a seed of its own); units never cross ranks, so the path
@@ -258,13 +294,15 @@ def run_ours(args, w, rank, world, device):
     side = torch.cuda.Stream()
     fork = torch.cuda.Event()
 
+    issue_step = DecodeStep(ctx, K, V, B, idx, cnt, out, one_call, s)
+
     def decode_loop(sync_incremental):
         """Every decode step of the job: append the step's K/V row, cluster the
         last m tokens every m steps (on a side stream overlapping the step,
         committed before the next one; or inline), then the decode step."""
-        commit_at = -1
-        for t in range(T):
-            ckv.append_kv(Knew[:, t:t + 1], Vnew[:, t:t + 1], K, V, L + t, stream=s)
+        state = {"commit_at": -1}
+
+        def incremental(t):
             if t > 0 and t % w.m == 0:
                 if sync_incremental:
                     ctx.cluster_incremental(K, L + t - w.m, stream=s)
@@ -272,14 +310,12 @@ def run_ours(args, w, rank, world, device):
                     fork.record(s)
                     side.wait_event(fork)
                     ctx.cluster_incremental_begin(K, L + t - w.m, stream=side)
-                    commit_at = t + 1
-            if t == commit_at:
+                    state["commit_at"] = t + 1
+            if t == state["commit_at"]:
                 ctx.cluster_incremental_commit(stream=s)
-            if one_call:
-                ctx.decode_step(Q[t], K, V, B, L + t + 1, idx, cnt, out, stream=s)
-            else:
-                ctx.select(Q[t], B, idx, cnt, stream=s)
-                ctx.sparse_decode_attn(Q[t], K, V, idx, cnt, B, L + t + 1, out, stream=s)
+
+        for t in range(T):
+            issue_step(Q[t], Knew[:, t:t + 1], Vnew[:, t:t + 1], L + t, L + t + 1, lambda: incremental(t))
 
     g_pre, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     # per step: append, score, select, attention, combine (either path); plus
@@ -379,13 +415,10 @@ def time_decode_steps(ctx, w, K, V, Q, Knew, Vnew, one_call, n=64, p_first=129, 
     p_first = max(1, min(p_first, T - n + 1))  # short jobs: the steps that exist
     steps = [(p_first + i - 1, L + p_first + i) for i in range(n)]  # (row appended, cur_len)
 
+    issue = DecodeStep(ctx, K, V, B, idx, cnt, out, one_call, s)
+
     def step(t, row, cur):
-        ckv.append_kv(Knew[:, row:row + 1], Vnew[:, row:row + 1], K, V, L + row, stream=s)
-        if one_call:
-            ctx.decode_step(Q[t], K, V, B, cur, idx, cnt, out, stream=s)
-        else:
-            ctx.select(Q[t], B, idx, cnt, stream=s)
-            ctx.sparse_decode_attn(Q[t], K, V, idx, cnt, B, cur, out, stream=s)
+        issue(Q[t], Knew[:, row:row + 1], Vnew[:, row:row + 1], L + row, cur)
 
     def timed(body):
         g = torch.cuda.CUDAGraph()
@@ -1006,7 +1039,9 @@ def main():
                        f"({w.units} units), d={w.d}, GQA {w.g}, prompt L={w.L}, {w.decode_steps} decode "
                        f"steps, B={w.B}, C={w.C} + {w.c_plus} every {w.m} steps, {w.iters} Lloyd iterations",
            "units": w.units, "L": w.L, "decode_steps": w.decode_steps, "B": w.B, "C": w.C,
-           "path": "ckv_decode_step" if args.path == "step" else "ckv_select + ckv_sparse_decode_attn",
+           "path": ("ckv_append_kv, then ckv_decode_step" if args.path == "step" else
+                    "ckv_append_kv on a side stream (joined before the attention) beside ckv_select, "
+                    "then ckv_sparse_decode_attn"),
            "incremental": "inline before the step" if args.sync_incremental else
                           "side stream: begun at the step, overlapping it; committed before the next step",
            "l2": (f"inputs larger than L2: {2 * w.units * w.max_len * w.d * 2 / 1e9:.1f} GB of K/V and "

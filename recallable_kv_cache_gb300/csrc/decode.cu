@@ -200,9 +200,12 @@ __global__ void __launch_bounds__(1024, 1) sel_kernel(
 
     // ---- 3. fast path: the 32 highest-ranked clusters.  Warp w sorts the E
     // lists of 32 keys it owns (in registers; sk keeps its order) and merges
-    // them into its 32 smallest keys; warp 0 merges the warps' lists in four
-    // independent chains.  If those 32 clusters hold min(B, total) tokens, the
-    // selection is a prefix of them and the rest of the ranking is not needed.
+    // them into its 32 smallest keys; then a merge tree across the warps: at
+    // each level the lower half of the remaining lists takes in the upper
+    // half (one merge per warp, all warps of a level at once), while the last
+    // warp sums the sizes.  If those 32 clusters hold min(B, total) tokens,
+    // the selection is a prefix of them and the rest of the ranking is not
+    // needed.
     __shared__ int s_fast, s_nsel, s_total;
     uint64_t* part = reinterpret_cast<uint64_t*>(start);  // [nwarps][32] (start/cl reused)
     {
@@ -213,19 +216,23 @@ __global__ void __launch_bounds__(1024, 1) sel_kernel(
         part[32 * warp + lane] = top;
     }
     __syncthreads();
-    if (warp == 0) {
+    if (warp == nwarps - 1) {  // never merges: nwarps >= 4, the tree's warps are below nwarps / 2
         int tot = 0;  // clustered tokens: the sum of all sizes
         for (int c = lane; c < C; c += 32) tot += szc[c];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(FULL, tot, o);
-        uint64_t ch[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) ch[k] = k < nwarps ? part[32 * k + lane] : ~0ull;
-        for (int l = 4; l < nwarps; l += 4)
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                if (l + k < nwarps) ch[k] = warp_merge32(ch[k], part[32 * (l + k) + lane], lane);
-        const uint64_t top = warp_merge32(warp_merge32(ch[0], ch[1], lane), warp_merge32(ch[2], ch[3], lane), lane);
+        if (lane == 0) s_total = tot;
+    }
+    for (int n = nwarps; n > 1; n >>= 1) {
+        if (warp < n / 2) {
+            const uint64_t a = part[32 * warp + lane], b = part[32 * (warp + n / 2) + lane];
+            part[32 * warp + lane] = warp_merge32(a, b, lane);
+        }
+        __syncthreads();
+    }
+    if (warp == 0) {
+        const int tot = s_total;
+        const uint64_t top = part[lane];
         const int target = tot < B ? tot : B;
         const int c = (int)(uint32_t)top;
         const int sz = (top != ~0ull && c < C) ? szc[c] : 0;
@@ -247,7 +254,6 @@ __global__ void __launch_bounds__(1024, 1) sel_kernel(
         if (lane == 0) {
             s_fast = fast;
             s_nsel = nsel;
-            s_total = tot;
         }
     }
     __syncthreads();
@@ -460,25 +466,41 @@ __global__ void __launch_bounds__(1024, 1) sel_kernel(
 
     }  // histogram path
 
-    // ---- 5. cut at the budget and compact the token ids
+    // ---- 5. cut at the budget and compact the token ids: FILL slots per
+    // thread at a time, their positions first, then all their permutation
+    // loads in flight together
     const int cnt = total < B ? total : B;
     if (tid == 0) count[u] = cnt;
     const int32_t* pu = perm + (size_t)u * ntok;
     int32_t* out = idx + (size_t)u * B;
-    for (int p = tid; p < cnt; p += NT) {
-        // largest rank r with start[r] <= p (that cluster is non-empty and holds p)
-        int lo = 0, hi = nsorted - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (start[mid] <= p) lo = mid;
-            else hi = mid - 1;
+    constexpr int FILL = 4;
+    for (int p0 = 0; p0 < cnt; p0 += FILL * NT) {
+        int pos[FILL];
+#pragma unroll
+        for (int f = 0; f < FILL; ++f) {
+            const int p = p0 + f * NT + tid;
+            pos[f] = -1;
+            if (p < cnt) {
+                // largest rank r with start[r] <= p (that cluster is non-empty and holds p)
+                int lo = 0, hi = nsorted - 1;
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (start[mid] <= p) lo = mid;
+                    else hi = mid - 1;
+                }
+                pos[f] = offc[cl[lo]] + (p - start[lo]);
+            }
         }
-        const int pos = offc[cl[lo]] + (p - start[lo]);
-        if ((unsigned)pos < (unsigned)ntok) {
-            out[p] = pu[pos];
-        } else {
-            set_err(dev_err, CKV_DEV_BAD_CSR);
-            out[p] = 0;
+        int32_t tok[FILL];
+#pragma unroll
+        for (int f = 0; f < FILL; ++f) tok[f] = (unsigned)pos[f] < (unsigned)ntok ? pu[pos[f]] : 0;
+#pragma unroll
+        for (int f = 0; f < FILL; ++f) {
+            const int p = p0 + f * NT + tid;
+            if (p < cnt) {
+                if ((unsigned)pos[f] >= (unsigned)ntok) set_err(dev_err, CKV_DEV_BAD_CSR);
+                out[p] = tok[f];
+            }
         }
     }
 }

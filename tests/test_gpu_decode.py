@@ -256,13 +256,11 @@ def test_decode_step_equals_select_then_attention(case):
 
 @pytest.mark.parametrize("C", [13, 129, 409, 1000])
 def test_decode_step_selection_edge_cases(C):
-    """ckv_decode_step selects inside its attention kernel (one warp per unit,
-    a size-weighted radix select over the score bits, then a sort of the
-    clusters that can be taken).  Against the oracle, given the GPU's own
-    scores: random cluster layouts with empty clusters, duplicated centroids
-    (tied scores), a zero query (every score tied: rank by cluster index),
-    budgets 0, 1, ragged, at and above the clustered tokens; the attention
-    over the selection against the oracle."""
+    """ckv_decode_step's selection equals ckv_select's, and both the oracle's
+    given the GPU's own scores: random cluster layouts with empty clusters,
+    duplicated centroids (tied scores), a zero query (every score tied: rank
+    by cluster index), budgets 0, 1, ragged, at and above the clustered
+    tokens; the step's attention over that selection against the oracle."""
     torch.cuda.init()
     U, g, d, pend = 3, 4, 128, 21
     rng = np.random.default_rng(1000 + C)
