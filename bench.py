@@ -65,6 +65,8 @@ def parse():
     p.add_argument("--decode-steps", type=int, default=0, help="override the decode steps (profiling)")
     p.add_argument("--sync-incremental", action="store_true",
                    help="cluster the new tokens inline instead of on a side stream overlapping the next step")
+    p.add_argument("--no-l2-persist", action="store_true",
+                   help="leave the centroid scoring copy and perm out of a persisting L2 set-aside")
     p.add_argument("--path", choices=["separate", "step"], default="separate",
                    help="decode step as ckv_select + ckv_sparse_decode_attn, or one "
                         "ckv_decode_step call")
@@ -282,6 +284,8 @@ def run_ours(args, w, rank, world, device):
     torch.cuda.synchronize()
     ctx = ckv.Context(units=U, g=w.g, max_len=w.max_len, max_clusters=w.max_clusters, max_budget=B,
                       iters=w.iters, m=w.m, c_plus=w.c_plus)
+    if not args.no_l2_persist:
+        ctx.set_l2_persistence(-1)  # the tables every step re-reads stay in L2
     idx = torch.empty(U, B, dtype=torch.int32, device="cuda")
     cnt = torch.empty(U, dtype=torch.int32, device="cuda")
     out = torch.empty(U, w.g, w.d, dtype=torch.float32, device="cuda")
@@ -887,8 +891,8 @@ def run_e2e(ctx, w, K, V, Q, one_call=False, sync_incremental=False):
 OTHER_WORKLOADS = ("tiny_2k", "layer_32k", "batch16_32k", "long_128k")
 
 
-def measure_workload(name, hbm, reps=2):
-    """One workload of the survey's set on this GPU, beside the main line:
+def measure_workload(name, hbm, reps=2, l2_persist=True):
+    """One of the other workloads on this GPU, beside the main line:
     prefill clustering of every unit (CUDA events, after a warm-up run) and
     K-means ms per layer; for the decode loops (batch16_32k, long_128k) the
     whole decode loop of the job as one CUDA graph (append the step's K/V row,
@@ -903,6 +907,8 @@ def measure_workload(name, hbm, reps=2):
     Q = synth.make_queries(w, w.n_queries if w.decode_steps == 0 else T, device="cuda")
     ctx = ckv.Context(units=U, g=w.g, max_len=w.max_len, max_clusters=w.max_clusters, max_budget=B,
                       kv_dtype=w.dtype, iters=w.iters, m=w.m, c_plus=w.c_plus)
+    if l2_persist:
+        ctx.set_l2_persistence(-1)
     s = torch.cuda.Stream()
     e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
     res = {"units": U, "L": L, "B": B, "C": w.C, "dtype": w.dtype}
@@ -1047,7 +1053,10 @@ def main():
            "l2": (f"inputs larger than L2: {2 * w.units * w.max_len * w.d * 2 / 1e9:.1f} GB of K/V and "
                   f"{w.decode_steps * w.units * w.g * w.d * 2 / 1e6:.0f} MB of queries resident; a decode step "
                   f"gathers ~{decode_bytes(w, w.decode_steps // 2, w.C, True)[0] / 1e6:.0f} MB of scattered rows "
-                  f"(L2 is 129 MB); no flush")}
+                  f"(L2 is 129 MB); no flush" +
+                  ("" if args.no_l2_persist else
+                   "; the centroid scoring copy and perm, which every step re-reads, in a persisting L2 "
+                   "set-aside (ckv_set_l2_persistence)"))}
 
     if args.impl == "reference":
         if rank != 0:
@@ -1153,7 +1162,7 @@ def main():
         # the main workload's tensors go first: the batch-16 and 128k jobs hold ~69 GB each
         r.clear()
         torch.cuda.empty_cache()
-        line["workloads"] = {n: measure_workload(n, hbm) for n in OTHER_WORKLOADS}
+        line["workloads"] = {n: measure_workload(n, hbm, l2_persist=not args.no_l2_persist) for n in OTHER_WORKLOADS}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

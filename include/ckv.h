@@ -372,6 +372,24 @@ ckv_status ckv_import_clusters(ckv_ctx* ctx, int32_t n_clusters, int32_t cluster
  * Errors: CKV_ERR_ARG. */
 ckv_status ckv_set_wait_limit(ckv_ctx* ctx, int64_t cycles, int32_t stall);
 
+/* L2 residency of the data every decode step re-reads (a GB300 has 129 MB of
+ * L2; the gathered K/V rows of one step are larger and have no reuse, so
+ * without this they evict the rest each step).  bytes > 0 sets aside up to
+ * that many bytes of L2 for persisting lines (capped at the device maximum),
+ * bytes < 0 sets aside what the context needs (the bf16 / fp32 scoring copy
+ * of the centroids, [units][max_clusters][d], and the label-sorted token ids
+ * perm, [units][max_len - sinks] int32), bytes = 0 turns it off.  While it is
+ * on, the scoring kernel reads the centroid copy and the selection kernel
+ * reads perm through access-policy windows whose hits persist (hit ratio =
+ * set-aside / bytes needed, at most 1).  The set-aside is the calling
+ * process's CUDA-context limit cudaLimitPersistingL2CacheSize on the current
+ * device: it is released with that context, the value found before the first
+ * call is restored by bytes = 0 and by ckv_destroy, and the persisting lines
+ * are reset then.  Results do not change.
+ * Errors: CKV_ERR_ARG (ctx null), CKV_ERR_CUDA (the limit could not be set,
+ * e.g. the device has no persisting L2). */
+ckv_status ckv_set_l2_persistence(ckv_ctx* ctx, int64_t bytes);
+
 /* Synchronises the context's last stream and reads then clears the device
  * error word (CKV_DEV_*). */
 ckv_status ckv_get_device_error(ckv_ctx* ctx, int32_t* code);

@@ -46,6 +46,7 @@ SIGNATURES = {
     "ckv_import_clusters": ([_P, _I, _I, _P, _P, _P, _P, _P], _I),
     "ckv_get_device_error": ([_P, ctypes.POINTER(_I)], _I),
     "ckv_set_wait_limit": ([_P, ctypes.c_int64, _I], _I),
+    "ckv_set_l2_persistence": ([_P, ctypes.c_int64], _I),
     "ckv_sparse_decode_attn_noalloc": ([_P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P], _I),
 }
 
@@ -276,6 +277,12 @@ class Context:
         """Bounded-wait limit of this context's kernels, and the failure
         detection test switch (see ckv_set_wait_limit)."""
         _check(lib().ckv_set_wait_limit(self.handle, int(cycles), 1 if stall else 0), "ckv_set_wait_limit")
+
+    def set_l2_persistence(self, nbytes: int = -1):
+        """L2 set-aside for the centroid scoring copy and perm, which every
+        decode step re-reads (see ckv_set_l2_persistence): -1 = what the
+        context needs, 0 = off."""
+        _check(lib().ckv_set_l2_persistence(self.handle, int(nbytes)), "ckv_set_l2_persistence")
 
     def device_error(self) -> int:
         v = ctypes.c_int32()

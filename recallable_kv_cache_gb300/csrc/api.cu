@@ -40,6 +40,17 @@ void free_all(ckv_ctx* c) {
     if (c->pend_done) cudaEventDestroy(c->pend_done);
 }
 
+// turns the persisting set-aside off and puts back the limit found before
+cudaError_t l2_release(ckv_ctx* ctx) {
+    if (!ctx->l2_saved) return cudaSuccess;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaCtxResetPersistingL2Cache();
+    if (e == cudaSuccess) e = cudaDeviceSetLimit(cudaLimitPersistingL2CacheSize, ctx->l2_prev_limit);
+    ctx->l2_on = 0;
+    ctx->l2_saved = 0;
+    return e;
+}
+
 ckv_status check_kv(const ckv_ctx* ctx, const void* K) {
     if (!ctx || !K) return CKV_ERR_ARG;
     if (!aligned16(K)) return CKV_ERR_ALIGN;
@@ -155,6 +166,7 @@ ckv_status ckv_destroy(ckv_ctx* ctx) {
     CKV_TRACE("ckv_destroy");
     if (!ctx) return CKV_ERR_ARG;
     cudaDeviceSynchronize();
+    l2_release(ctx);
     free_all(ctx);
     delete ctx;
     return CKV_OK;
@@ -445,6 +457,45 @@ ckv_status ckv_set_wait_limit(ckv_ctx* ctx, int64_t cycles, int32_t stall) {
     if (cycles < 1 || cycles > MAX_WAIT_LIMIT || (stall != 0 && stall != 1)) return CKV_ERR_ARG;
     ctx->wait_limit = cycles;
     ctx->stall = stall;
+    return CKV_OK;
+}
+
+ckv_status ckv_set_l2_persistence(ckv_ctx* ctx, int64_t bytes) {
+    CKV_TRACE("ckv_set_l2_persistence");
+    if (!ctx) return CKV_ERR_ARG;
+    if (bytes == 0) return cuda_status(l2_release(ctx));
+    int maxp = 0, maxw = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&maxp, cudaDevAttrMaxPersistingL2CacheSize, ctx->device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&maxw, cudaDevAttrMaxAccessPolicyWindowSize, ctx->device);
+    if (e != cudaSuccess || maxp <= 0 || maxw <= 0) return CKV_ERR_CUDA;
+    const size_t U = (size_t)ctx->cfg.units;
+    const size_t mu_bytes = U * ctx->cmax * D * ctx->elem;
+    const size_t perm_bytes = U * ctx->ntok * sizeof(int32_t);
+    const size_t need = mu_bytes + perm_bytes;
+    size_t want = bytes < 0 ? need : (size_t)bytes;
+    if (want > (size_t)maxp) want = (size_t)maxp;
+    if (!ctx->l2_saved) {
+        if ((e = cudaDeviceGetLimit(&ctx->l2_prev_limit, cudaLimitPersistingL2CacheSize)) != cudaSuccess)
+            return CKV_ERR_CUDA;
+        ctx->l2_saved = 1;
+    }
+    if ((e = cudaDeviceSetLimit(cudaLimitPersistingL2CacheSize, want)) != cudaSuccess) return CKV_ERR_CUDA;
+    size_t got = 0;
+    if ((e = cudaDeviceGetLimit(&got, cudaLimitPersistingL2CacheSize)) != cudaSuccess) return CKV_ERR_CUDA;
+    // both windows share the set-aside: each hit ratio is set-aside / bytes needed
+    const float hit = got >= need ? 1.0f : (float)((double)got / (double)need);
+    auto window = [&](void* base, size_t n) {
+        cudaAccessPolicyWindow w = {};
+        w.base_ptr = base;
+        w.num_bytes = n < (size_t)maxw ? n : (size_t)maxw;
+        w.hitRatio = hit;
+        w.hitProp = cudaAccessPropertyPersisting;
+        w.missProp = cudaAccessPropertyStreaming;
+        return w;
+    };
+    ctx->l2_mu = window(ctx->mu_s, mu_bytes);
+    ctx->l2_perm = window(ctx->perm, perm_bytes);
+    ctx->l2_on = 1;
     return CKV_OK;
 }
 

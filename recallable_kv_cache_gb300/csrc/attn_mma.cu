@@ -296,6 +296,9 @@ __global__ void __launch_bounds__(MW * 32, 1) attn_mma_kernel(const MmaArgs a) {
 // independent, so they are in flight together.
 constexpr int CMB_MAX_SLOTS = 256;
 constexpr int CMB_REG_SLOTS = 12;  // units with at most this many partials merge in registers
+// dynamic shared memory of a combine CTA: with the attention CTA's 209 KB it
+// exceeds an SM's 228 KB
+constexpr int CMB_BLOCK_SMEM = 64 * 1024;
 
 template <int G>
 __global__ void __launch_bounds__(G * D) attn_mma_combine_kernel(const float* __restrict__ part, int tpu, int tpw,
@@ -305,6 +308,7 @@ __global__ void __launch_bounds__(G * D) attn_mma_combine_kernel(const float* __
     __shared__ float lw[CMB_MAX_SLOTS][G];
     __shared__ float Ls[G];
     const int u = blockIdx.x, tid = threadIdx.x;
+    ptx::grid_dependency_wait();  // the partials come from the attention kernel
     const int w0 = (u * tpu) / tpw, w1 = (u * tpu + tpu - 1) / tpw;
     const int ns = min(w1 - w0 + 1, CMB_MAX_SLOTS);
     const float* pu = part + (size_t)u * max_slots * PW;
@@ -404,8 +408,14 @@ cudaError_t launch_mma_t(const void* q, const void* K, const void* V, const int3
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if ((e = launch_dependent(kern, dim3(grid), dim3(MW * 32), smem, st, a)) != cudaSuccess) return e;
-    attn_mma_combine_kernel<G><<<units, G * D, 0, st>>>(part, a.tpu, a.tpw, max_slots, out);
-    return cudaGetLastError();
+    // the combine is a dependent launch too, so its CTAs are resident as soon
+    // as SMs free up; its (unused) dynamic shared memory keeps it off any SM
+    // that still holds an attention CTA, whose warps it would slow
+    auto ck = attn_mma_combine_kernel<G>;
+    if ((e = cudaFuncSetAttribute(ck, cudaFuncAttributeMaxDynamicSharedMemorySize, CMB_BLOCK_SMEM)) != cudaSuccess)
+        return e;
+    return launch_dependent(ck, dim3(units), dim3(G * D), (size_t)CMB_BLOCK_SMEM, st, (const float*)part, a.tpu,
+                            a.tpw, max_slots, out);
 }
 
 }  // namespace

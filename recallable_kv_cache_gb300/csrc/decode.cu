@@ -999,12 +999,12 @@ cudaError_t launch_attn_t(const void* q, const void* K, const void* V, const int
 template <typename T>
 cudaError_t launch_score_t(const void* q, const void* mu, int g, int units, int cmax, int C,
                            float* scores, int stride, const int32_t* pf_sizes, const int32_t* pf_offsets,
-                           cudaStream_t s) {
+                           const cudaAccessPolicyWindow* win, cudaStream_t s) {
     constexpr int RPW = (32 / (D / Vec<T>::N)) * SCORE_UNROLL;  // rows per warp
     dim3 grid((C + 8 * RPW - 1) / (8 * RPW), units);
-#define CKV_SCORE(G)                                                                                     \
-    return launch_dependent(score_kernel<T, G>, grid, dim3(256), 0, s, (const T*)q, (const T*)mu, cmax, C, \
-                            scores, stride, pf_sizes, pf_offsets)
+#define CKV_SCORE(G)                                                                                          \
+    return launch_dependent_win(score_kernel<T, G>, grid, dim3(256), 0, s, win, (const T*)q, (const T*)mu, cmax, \
+                                C, scores, stride, pf_sizes, pf_offsets)
     switch (g) {
         case 1: CKV_SCORE(1);
         case 2: CKV_SCORE(2);
@@ -1022,9 +1022,10 @@ cudaError_t launch_sel_t(const ckv_ctx* ctx, const float* scores, int stride, in
     auto kern = sel_kernel<E>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_dependent(kern, dim3(ctx->cfg.units), dim3(N / E), smem, s, scores, stride, ctx->cmax, C, N,
-                            (const int32_t*)ctx->sizes, (const int32_t*)ctx->offsets, (const int32_t*)ctx->perm,
-                            ctx->ntok, B, idx, count, ctx->dev_err);
+    return launch_dependent_win(kern, dim3(ctx->cfg.units), dim3(N / E), smem, s,
+                                ctx->l2_on ? &ctx->l2_perm : nullptr, scores, stride, ctx->cmax, C, N,
+                                (const int32_t*)ctx->sizes, (const int32_t*)ctx->offsets,
+                                (const int32_t*)ctx->perm, ctx->ntok, B, idx, count, ctx->dev_err);
 }
 
 }  // namespace
@@ -1034,11 +1035,12 @@ cudaError_t launch_score(const ckv_ctx* ctx, const void* q, int C, float* scores
     if (C <= 0) return cudaSuccess;
     const int32_t* ps = prefetch_csr ? ctx->sizes : nullptr;
     const int32_t* po = prefetch_csr ? ctx->offsets : nullptr;
+    const cudaAccessPolicyWindow* win = ctx->l2_on ? &ctx->l2_mu : nullptr;
     if (ctx->cfg.kv_dtype == CKV_BF16)
         return launch_score_t<__nv_bfloat16>(q, ctx->mu_s, ctx->cfg.g, ctx->cfg.units, ctx->cmax, C,
-                                             scores, stride, ps, po, s);
+                                             scores, stride, ps, po, win, s);
     return launch_score_t<float>(q, ctx->mu_s, ctx->cfg.g, ctx->cfg.units, ctx->cmax, C, scores,
-                                 stride, ps, po, s);
+                                 stride, ps, po, win, s);
 }
 
 cudaError_t launch_select(const ckv_ctx* ctx, const void* q, const float* scores, int stride, int C, int B,

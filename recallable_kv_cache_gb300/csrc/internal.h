@@ -33,18 +33,29 @@ inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
 // while the previous kernel of the stream is still running; it must call
 // ptx::grid_dependency_wait() before touching memory that kernel writes.
 template <typename... P, typename... A>
-cudaError_t launch_dependent(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, A&&... args) {
+cudaError_t launch_dependent_win(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                 const cudaAccessPolicyWindow* win, A&&... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute at[1];
+    cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     at[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = at;
     cfg.numAttrs = 1;
+    if (win) {
+        // accesses of this launch inside the window: hits persist in L2
+        at[1].id = cudaLaunchAttributeAccessPolicyWindow;
+        at[1].val.accessPolicyWindow = *win;
+        cfg.numAttrs = 2;
+    }
+    cfg.attrs = at;
     return cudaLaunchKernelEx(&cfg, kern, static_cast<A&&>(args)...);
+}
+template <typename... P, typename... A>
+cudaError_t launch_dependent(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, A&&... args) {
+    return launch_dependent_win(kern, grid, block, smem, s, nullptr, static_cast<A&&>(args)...);
 }
 inline int ceil_div(int x, int m) { return (x + m - 1) / m; }
 
@@ -91,6 +102,12 @@ struct ckv_ctx {
     float* assign_best; // [U][ntok] running arg-max values between assignment passes (large C only)
     long long wait_limit; // SM cycles before a bounded device wait gives up
     int stall;            // failure detection test: kernels first wait on something nothing completes
+    // L2 persistence (ckv_set_l2_persistence): windows for the scoring copy
+    // and perm while l2_on; the context limit found before the first call
+    int l2_on;
+    int l2_saved;
+    size_t l2_prev_limit;
+    cudaAccessPolicyWindow l2_mu, l2_perm;
 };
 
 namespace ckv {

@@ -91,3 +91,8 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
 
 def test_set_wait_limit_rejects_on_host(lib):
     assert lib.ckv_set_wait_limit(None, 1000, 0) == -1
+
+
+def test_set_l2_persistence_rejects_on_host(lib):
+    assert lib.ckv_set_l2_persistence(None, -1) == -1
+    assert lib.ckv_set_l2_persistence(None, 0) == -1

@@ -226,6 +226,39 @@ def test_select_large_cluster_counts(C):
     ctx.close()
 
 
+def test_l2_persistence_changes_no_result(case):
+    """With the centroid copy and perm held in a persisting L2 set-aside
+    (ckv_set_l2_persistence) the selection and the attention give exactly
+    the results they give without it; turning it on twice and off again is
+    accepted."""
+    w, ctx = case["w"], case["ctx"]
+    pend = CASES[case["name"]][5]
+    q = case["Q"][0].cuda().contiguous()
+    cur_len = w.L + pend
+
+    def run():
+        i = torch.full((w.units, w.B), -3, dtype=torch.int32, device="cuda")
+        c = torch.empty(w.units, dtype=torch.int32, device="cuda")
+        o = torch.empty(w.units, w.g, 128, dtype=torch.float32, device="cuda")
+        ctx.decode_step(q, case["Kd"], case["Vd"], w.B, cur_len, i, c, o)
+        torch.cuda.synchronize()
+        return i, c, o
+
+    i0, c0, o0 = run()
+    try:
+        ctx.set_l2_persistence(-1)
+        ctx.set_l2_persistence(1 << 20)
+        i1, c1, o1 = run()
+        ctx.set_l2_persistence(-1)
+        i2, c2, o2 = run()
+    finally:
+        ctx.set_l2_persistence(0)
+    i3, c3, o3 = run()
+    assert ctx.device_error() == 0
+    for i, c, o in ((i1, c1, o1), (i2, c2, o2), (i3, c3, o3)):
+        assert torch.equal(c, c0) and torch.equal(i, i0) and torch.equal(o, o0)
+
+
 def test_decode_step_equals_select_then_attention(case):
     """ckv_decode_step (selection then attention in one call) gives the idx /
     count of ckv_select and the output of ckv_sparse_decode_attn; three steps
