@@ -1,7 +1,8 @@
 // Decode-step kernels of the ClusterKV path:
 //   score_kernel   cluster scores q . mu (section "Selection at semantic-cluster
 //                  granularity"), HBM-bound stream over the centroid table;
-//   sel_kernel     rank clusters, prefix-sum their sizes, trim the last one and
+//   sel_kernel     (scores of the unit's clusters, up to 1024 of them,) rank
+//                  clusters, prefix-sum their sizes, trim the last one and
 //                  compact the token ids (section "Selection and indexing
 //                  mechanism", Fig. 8), one CTA per unit;
 //   attn_kernel    gather of the selected K/V rows with bulk-async copies into
@@ -148,8 +149,9 @@ __device__ __forceinline__ uint64_t rank_key(float s, int c) {
     return ((uint64_t)(~ord) << 32) | (uint32_t)c;                      // descending score, asc c
 }
 
-// One CTA per unit.  Scores (from score_kernel or the caller) become 64-bit
-// keys (descending score, ascending cluster index) that are sorted by a
+// One CTA per unit.  Scores (computed by the CTA itself from q and the
+// centroid copy up to 1024 clusters, else from score_kernel or the caller)
+// become 64-bit keys (descending score, ascending cluster index) that are sorted by a
 // bitonic network held in registers: exchange distances below 32 use warp
 // shuffles, larger ones shared memory, and distances of at least the block
 // size stay inside a thread (E keys per thread).  The sizes taken in rank
@@ -157,17 +159,80 @@ __device__ __forceinline__ uint64_t rank_key(float s, int c) {
 // p < min(B, total) looks up its rank by binary search and copies its token id
 // from the label-sorted permutation.  The sizes, offsets and scores are all
 // loaded before any of them is used, so they share one round trip.
-template <int E>
+// Scores of every cluster of unit u computed inside the selection's CTA
+// (the same arithmetic as score_kernel, so the same bits): q summed over the
+// g heads, then per centroid row LPR lanes take CPL channels each (fma chain
+// in channel order) and a shuffle reduction over the row's lanes.  Rows are
+// read in rounds of SEL_SCORE_UNROLL rows per lane group, the next round's
+// loads in flight while the current one is reduced; the scores land in
+// shared memory.
+constexpr int SEL_SCORE_UNROLL = 4;
+template <typename T, int G>
+__device__ __forceinline__ void score_unit(const T* __restrict__ q, const T* __restrict__ mu, int u, int cmax,
+                                           int C, float* scs, int lane, int warp, int nwarps) {
+    constexpr int CPL = Vec<T>::N;   // channels per lane
+    constexpr int LPR = D / CPL;     // lanes per centroid row
+    constexpr int RPI = 32 / LPR;    // rows per warp-wide load
+    constexpr int UN = SEL_SCORE_UNROLL;
+    const int sub = lane / LPR, li = lane % LPR;
+    float qs[CPL];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) qs[c] = 0.f;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        const uint4 w = *reinterpret_cast<const uint4*>(q + ((size_t)u * G + h) * D + li * CPL);
+        float f[CPL];
+        Vec<T>::unpack(w, f);
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) qs[c] += f[c];
+    }
+    const T* mu_u = mu + (size_t)u * cmax * D + li * CPL;
+    const int per_round = nwarps * RPI * UN;
+    auto row_of = [&](int r0, int i) { return r0 + (i * nwarps + warp) * RPI + sub; };
+    auto load = [&](int r0, uint4 (&v)[UN]) {
+#pragma unroll
+        for (int i = 0; i < UN; ++i) {
+            const int r = row_of(r0, i);
+            v[i] = r < C ? *reinterpret_cast<const uint4*>(mu_u + (size_t)r * D) : make_uint4(0, 0, 0, 0);
+        }
+    };
+    uint4 cur[UN], nxt[UN];
+    load(0, cur);
+    for (int r0 = 0; r0 < C; r0 += per_round) {
+        if (r0 + per_round < C) load(r0 + per_round, nxt);
+#pragma unroll
+        for (int i = 0; i < UN; ++i) {
+            float f[CPL];
+            Vec<T>::unpack(cur[i], f);
+            float dot = 0.f;
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) dot = fmaf(qs[c], f[c], dot);
+#pragma unroll
+            for (int o = LPR / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(FULL, dot, o);
+            const int r = row_of(r0, i);
+            if (li == 0 && r < C) scs[r] = dot;
+        }
+#pragma unroll
+        for (int i = 0; i < UN; ++i) cur[i] = nxt[i];
+    }
+}
+
+// G == 0: scores_in [units][sstride] are given.  G > 0: the scores are
+// computed here from q [units][G][D] and the scoring copy mu [units][cmax][D]
+// of type T.
+template <int E, typename T, int G>
 __global__ void __launch_bounds__(1024, 1) sel_kernel(
-    const float* __restrict__ scores_in, int sstride, int cmax, int C, int N, const int32_t* __restrict__ sizes,
-    const int32_t* __restrict__ offsets, const int32_t* __restrict__ perm, int ntok, int B,
-    int32_t* __restrict__ idx, int32_t* __restrict__ count, int32_t* __restrict__ dev_err) {
+    const float* __restrict__ scores_in, int sstride, const T* __restrict__ q, const T* __restrict__ mu, int cmax,
+    int C, int N, const int32_t* __restrict__ sizes, const int32_t* __restrict__ offsets,
+    const int32_t* __restrict__ perm, int ntok, int B, int32_t* __restrict__ idx, int32_t* __restrict__ count,
+    int32_t* __restrict__ dev_err) {
     extern __shared__ __align__(16) unsigned char sel_smem[];
     uint64_t* sk = reinterpret_cast<uint64_t*>(sel_smem);  // [N]
     int32_t* start = reinterpret_cast<int32_t*>(sk + N);   // [N]
     int32_t* cl = start + N;                               // [N]
     int32_t* szc = cl + N;                                 // [N] sizes by cluster
     int32_t* offc = szc + N;                               // [N] offsets by cluster
+    float* scs = reinterpret_cast<float*>(offc + N);       // [N] scores computed here (the histogram's space)
     __shared__ int32_t wsum[32];
     __shared__ int32_t s_tot;
     const int u = blockIdx.x, tid = threadIdx.x, NT = blockDim.x;
@@ -183,7 +248,16 @@ __global__ void __launch_bounds__(1024, 1) sel_kernel(
         const int c = e * NT + tid;
         szr[e] = c < C ? sizes[(size_t)u * cmax + c] : 0;
         ofr[e] = c < C ? offsets[(size_t)u * (cmax + 1) + c] : 0;
-        scr[e] = c < C ? scores_in[(size_t)u * sstride + c] : 0.f;
+        if constexpr (G == 0) scr[e] = c < C ? scores_in[(size_t)u * sstride + c] : 0.f;
+    }
+    if constexpr (G > 0) {
+        score_unit<T, G>(q, mu, u, cmax, C, scs, lane, warp, nwarps);
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const int c = e * NT + tid;
+            scr[e] = c < C ? scs[c] : 0.f;
+        }
     }
     // ---- 2. unsorted keys (N is a multiple of NT: every slot is written)
 #pragma unroll
@@ -1015,17 +1089,46 @@ cudaError_t launch_score_t(const void* q, const void* mu, int g, int units, int 
     return cudaErrorInvalidValue;
 }
 
-template <int E>
-cudaError_t launch_sel_t(const ckv_ctx* ctx, const float* scores, int stride, int C, int N, int B, int32_t* idx,
-                         int32_t* count, cudaStream_t s) {
-    const size_t smem = (size_t)N * 24 + (size_t)4096 * 4;
-    auto kern = sel_kernel<E>;
+template <int E, typename T, int G>
+cudaError_t launch_sel_t(const ckv_ctx* ctx, const float* scores, int stride, const void* q, int C, int N, int B,
+                         int32_t* idx, int32_t* count, cudaStream_t s) {
+    // keys, starts, ranks, sizes, offsets; then the histogram (or the scores computed here)
+    const size_t smem = (size_t)N * 24 + (size_t)(N > 4096 ? N : 4096) * 4;
+    auto kern = sel_kernel<E, T, G>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_dependent_win(kern, dim3(ctx->cfg.units), dim3(N / E), smem, s,
-                                ctx->l2_on ? &ctx->l2_perm : nullptr, scores, stride, ctx->cmax, C, N,
+    // the centroid copy is what this launch re-reads each step when it scores
+    const cudaAccessPolicyWindow* win = !ctx->l2_on ? nullptr : (G > 0 ? &ctx->l2_mu : &ctx->l2_perm);
+    return launch_dependent_win(kern, dim3(ctx->cfg.units), dim3(N / E), smem, s, win, scores, stride,
+                                static_cast<const T*>(q), static_cast<const T*>(ctx->mu_s), ctx->cmax, C, N,
                                 (const int32_t*)ctx->sizes, (const int32_t*)ctx->offsets,
                                 (const int32_t*)ctx->perm, ctx->ntok, B, idx, count, ctx->dev_err);
+}
+
+template <int E>
+cudaError_t launch_sel_e(const ckv_ctx* ctx, const float* scores, int stride, const void* q, int C, int N, int B,
+                         int32_t* idx, int32_t* count, cudaStream_t s) {
+    if (scores) return launch_sel_t<E, float, 0>(ctx, scores, stride, nullptr, C, N, B, idx, count, s);
+    if constexpr (E == 1) {  // scoring inside the selection: one key per thread only
+#define CKV_SEL(T, G) return launch_sel_t<E, T, G>(ctx, nullptr, 0, q, C, N, B, idx, count, s)
+        if (ctx->cfg.kv_dtype == CKV_BF16) {
+            switch (ctx->cfg.g) {
+                case 1: CKV_SEL(__nv_bfloat16, 1);
+                case 2: CKV_SEL(__nv_bfloat16, 2);
+                case 4: CKV_SEL(__nv_bfloat16, 4);
+                case 8: CKV_SEL(__nv_bfloat16, 8);
+            }
+        } else {
+            switch (ctx->cfg.g) {
+                case 1: CKV_SEL(float, 1);
+                case 2: CKV_SEL(float, 2);
+                case 4: CKV_SEL(float, 4);
+                case 8: CKV_SEL(float, 8);
+            }
+        }
+#undef CKV_SEL
+    }
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace
@@ -1045,20 +1148,21 @@ cudaError_t launch_score(const ckv_ctx* ctx, const void* q, int C, float* scores
 
 cudaError_t launch_select(const ckv_ctx* ctx, const void* q, const float* scores, int stride, int C, int B,
                           int32_t* idx, int32_t* count, cudaStream_t s) {
-    if (!scores) {
-        // scores of every cluster into the context's scratch (a many-CTA
-        // stream over the centroid table), then the selection reads them
+    int N = 128;
+    while (N < C) N <<= 1;
+    if (!scores && N > 1024) {
+        // many clusters: scores of every cluster into the context's scratch
+        // (a many-CTA stream over the centroid table), then the selection
+        // reads them; up to 1024 clusters each selection CTA scores its unit
         cudaError_t e = launch_score(ctx, q, C, ctx->scores, ctx->cmax, s, true);
         if (e != cudaSuccess) return e;
         scores = ctx->scores;
         stride = ctx->cmax;
     }
-    int N = 128;
-    while (N < C) N <<= 1;
-    if (N <= 1024) return launch_sel_t<1>(ctx, scores, stride, C, N, B, idx, count, s);
-    if (N == 2048) return launch_sel_t<2>(ctx, scores, stride, C, N, B, idx, count, s);
-    if (N == 4096) return launch_sel_t<4>(ctx, scores, stride, C, N, B, idx, count, s);
-    if (N == 8192) return launch_sel_t<8>(ctx, scores, stride, C, N, B, idx, count, s);
+    if (N <= 1024) return launch_sel_e<1>(ctx, scores, stride, q, C, N, B, idx, count, s);
+    if (N == 2048) return launch_sel_e<2>(ctx, scores, stride, q, C, N, B, idx, count, s);
+    if (N == 4096) return launch_sel_e<4>(ctx, scores, stride, q, C, N, B, idx, count, s);
+    if (N == 8192) return launch_sel_e<8>(ctx, scores, stride, q, C, N, B, idx, count, s);
     return cudaErrorInvalidValue;
 }
 
