@@ -35,17 +35,12 @@ from recallable_kv_cache_gb300 import synth  # noqa: E402
 
 METRIC = "sparse-decode tokens/s at 32k ctx, B=1024; K-means ms/layer; % of HBM roofline"
 
-# DRAM bytes (read + write) of one decode step (append, scoring, selection,
-# attention, combine) per algorithmic byte, from one ncu capture of the current
-# kernels on a 64-unit case (decode step 8, 42.61 MB algorithmic; DRAM reads
-# 0.046 + 6.98 + 0.72 + 34.74 + 2.96 MB, writes 0: ncu flushes the caches
-# between the serialised kernels, so the writes land after each kernel and the
-# combine reads its partials back from DRAM); the traffic of a full-size step
-# is this ratio times its algorithmic bytes.  None whenever a kernel changes
-# until it is captured again.
-STEP_TRAFFIC_PER_ALG_BYTE = 45.45e6 / 42.61e6
-STEP_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of the five kernels of one decode step, "
-                       "64-unit case, scaled by algorithmic bytes (profiles/decode_step_traffic_decode_32k.md)")
+# DRAM bytes (read + write) of one decode step (the kernels of one step) per
+# algorithmic byte, from one ncu capture of the current kernels on a 64-unit
+# case; the traffic of a full-size step is this ratio times its algorithmic
+# bytes.  None whenever a kernel changes until it is captured again.
+STEP_TRAFFIC_PER_ALG_BYTE = None
+STEP_TRAFFIC_SOURCE = "not captured for the current kernels"
 WORKLOAD = "decode_32k"
 
 
@@ -322,9 +317,11 @@ def run_ours(args, w, rank, world, device):
             issue_step(Q[t], Knew[:, t:t + 1], Vnew[:, t:t + 1], L + t, L + t + 1, lambda: incremental(t))
 
     g_pre, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-    # per step: append, score, select, attention, combine (either path); plus
-    # one incremental kernel per block
-    per_step = 5
+    # per step: append, selection (which scores up to 1024 clusters itself;
+    # above that a scoring kernel first), attention, combine (either path);
+    # plus one incremental kernel per block
+    C_max = w.C + w.c_plus * w.n_incremental
+    per_step = 4 if C_max <= 1024 else 5
     launches = {"prefill": 1 + w.iters * 6, "decode": per_step * T + w.n_incremental}
     with torch.cuda.stream(s):
         with torch.cuda.graph(g_pre, stream=s):
@@ -1101,7 +1098,7 @@ def main():
     step_bytes = r["decode_bytes_per_step"] + append_b
     step_us = 1000.0 * decode_ms / T
     decode_gbs = step_bytes / (step_us / 1e6) / 1e9
-    kernels = ("append_kv_kernel + score_kernel + sel_kernel + attn_mma_kernel + attn_mma_combine_kernel "
+    kernels = ("append_kv_kernel + sel_kernel (scoring and selection) + attn_mma_kernel + attn_mma_combine_kernel "
                "(ckv_append_kv + " + ("ckv_decode_step)" if r["one_call"] else
                                       "ckv_select + ckv_sparse_decode_attn)"))
     traffic_ratio = STEP_TRAFFIC_PER_ALG_BYTE

@@ -166,7 +166,7 @@ __device__ __forceinline__ uint64_t rank_key(float s, int c) {
 // read in rounds of SEL_SCORE_UNROLL rows per lane group, the next round's
 // loads in flight while the current one is reduced; the scores land in
 // shared memory.
-constexpr int SEL_SCORE_UNROLL = 4;
+constexpr int SEL_SCORE_UNROLL = 2;
 template <typename T, int G>
 __device__ __forceinline__ void score_unit(const T* __restrict__ q, const T* __restrict__ mu, int u, int cmax,
                                            int C, float* scs, int lane, int warp, int nwarps) {
