@@ -42,6 +42,7 @@ METRIC = "sparse-decode tokens/s at 32k ctx, B=1024; K-means ms/layer; % of HBM 
 STEP_TRAFFIC_PER_ALG_BYTE = None
 STEP_TRAFFIC_SOURCE = "not captured for the current kernels"
 WORKLOAD = "decode_32k"
+K_UPLOAD_STREAMS = 1  # the prompt's keys go up in this many concurrent copies
 
 
 def parse():
@@ -60,6 +61,10 @@ def parse():
     p.add_argument("--decode-steps", type=int, default=0, help="override the decode steps (profiling)")
     p.add_argument("--sync-incremental", action="store_true",
                    help="cluster the new tokens inline instead of on a side stream overlapping the next step")
+    p.add_argument("--e2e-copy-nodes", action="store_true",
+                   help="end-to-end run: copy each step's inputs and outputs instead of mapping host memory")
+    p.add_argument("--upload-streams", type=int, default=K_UPLOAD_STREAMS,
+                   help="concurrent copies for the prompt keys' upload in the end-to-end run")
     p.add_argument("--no-l2-persist", action="store_true",
                    help="leave the centroid scoring copy and perm out of a persisting L2 set-aside")
     p.add_argument("--path", choices=["separate", "step"], default="separate",
@@ -164,6 +169,22 @@ class ExternalEvents:
         if r != 0:
             raise RuntimeError(f"cudaMemcpy2DAsync failed: {r}")
 
+    def copy_prefix_h2d_split(self, dst: torch.Tensor, src: torch.Tensor, rows: int, stream: torch.cuda.Stream,
+                              streams, forks, joins):
+        """copy_prefix_h2d with the units cut into len(streams) groups, each
+        copied on its own stream (forked from and joined back into `stream`),
+        so that several copy engines share the host link."""
+        n, U = len(streams), src.shape[0]
+        forks[0].record(stream)
+        for i, st in enumerate(streams):
+            u0, u1 = U * i // n, U * (i + 1) // n
+            if u0 == u1:
+                continue
+            st.wait_event(forks[0])
+            self.copy_prefix_h2d(dst[u0:u1], src[u0:u1], rows, st)
+            joins[i].record(st)
+            stream.wait_event(joins[i])
+
     def copy_rows_h2d(self, dst: torch.Tensor, src: torch.Tensor, stream: torch.cuda.Stream):
         """src [n, w] contiguous pinned host -> dst [n, w] device view with a row
         stride: one cudaMemcpy2DAsync (rows land where the caller's layout wants
@@ -181,9 +202,11 @@ def decode_bytes(w, step: int, C: int, async_incr: bool = False, pend: int | Non
     """Algorithmic HBM bytes of decode step `step` for all units: (attention, whole step).
     Attention reads every attended K and V row once (256 B each in bf16, 512
     in fp32) for all g heads, the indices, q, and writes out (fp32).  Scoring
-    reads the centroid scoring copy and q, writes the scores; selection reads
-    scores, sizes, offsets and the selected perm entries, writes idx and
-    count.  `pend` overrides the pending tokens of the step."""
+    reads the centroid scoring copy and q; selection reads sizes, offsets and
+    the selected perm entries, writes idx and count.  Above 1024 clusters the
+    scores also go through memory (written by the scoring kernel, read by the
+    selection); up to that the selection CTA scores its own unit and they do
+    not.  `pend` overrides the pending tokens of the step."""
     U, g, d, B = w.units, w.g, w.d, w.B
     e = 4 if w.dtype == "f32" else 2
     if pend is None:
@@ -192,8 +215,9 @@ def decode_bytes(w, step: int, C: int, async_incr: bool = False, pend: int | Non
             pend += w.m  # the block being clustered on the side stream is still pending
     rows = w.sinks + pend + B
     attn = U * (rows * 2 * d * e + B * 4 + 4 + g * d * e + g * d * 4)
-    score = U * (C * d * e + g * d * e + C * 4)
-    select = U * (C * 4 + C * 4 + (C + 1) * 4 + B * 4 + B * 4 + 4)
+    scores_through_memory = 2 * C * 4 if C > 1024 else 0
+    score = U * (C * d * e + g * d * e)
+    select = U * (scores_through_memory + C * 4 + (C + 1) * 4 + B * 4 + B * 4 + 4)
     return attn, attn + score + select
 
 
@@ -392,7 +416,8 @@ def run_ours(args, w, rank, world, device):
     res["ctx"] = ctx
     res["tensors"] = (K, V, Q)
     if not args.no_e2e:
-        res["e2e"] = run_e2e(ctx, w, K, V, Q, one_call, args.sync_incremental)
+        res["e2e"] = run_e2e(ctx, w, K, V, Q, one_call, args.sync_incremental, args.upload_streams,
+                             args.e2e_copy_nodes)
     return res
 
 
@@ -728,7 +753,8 @@ def full_kv_attention(w, K, V, Q, reps=5):
             "what": "attention over all L tokens of every unit with the same kernel (idx = every prompt token)"}
 
 
-def run_e2e(ctx, w, K, V, Q, one_call=False, sync_incremental=False):
+def run_e2e(ctx, w, K, V, Q, one_call=False, sync_incremental=False, upload_streams=K_UPLOAD_STREAMS,
+            copy_nodes=False):
     """The same job through the public API from pinned host buffers: upload the
     prompt K/V, prefill clustering, then per decode step upload q and the new
     K/V row of every unit, select, attend, and read the output back.  The calls
@@ -763,6 +789,8 @@ def run_e2e(ctx, w, K, V, Q, one_call=False, sync_incremental=False):
     outs = [torch.empty(U, g, d, dtype=torch.float32, device="cuda") for _ in range(2)]
     s, side, up, dn, sk, sv = (torch.cuda.Stream() for _ in range(6))
     e_fork, e_v = torch.cuda.Event(), torch.cuda.Event()
+    k_streams = [torch.cuda.Stream() for _ in range(max(1, upload_streams))]
+    k_forks, k_joins = [torch.cuda.Event()], [torch.cuda.Event() for _ in k_streams]
     e_step = [torch.cuda.Event() for _ in range(T)]
     e_k = [torch.cuda.Event() for _ in range(T)]
     e_vr = [torch.cuda.Event() for _ in range(T)]
@@ -774,12 +802,22 @@ def run_e2e(ctx, w, K, V, Q, one_call=False, sync_incremental=False):
     ext = ExternalEvents()  # captured records become timing nodes
     # on unified-addressing systems (Grace: the C2C link) the kernels can read
     # and write pinned host memory directly, which saves the per-step copy nodes
-    zero_copy = ext.host_mapped(inp_h) and ext.host_mapped(outh)
+    zero_copy = not copy_nodes and ext.host_mapped(inp_h) and ext.host_mapped(outh)
     torch.cuda.synchronize()
+    # the host link as this machine gives it: one 1 GiB copy from pinned memory
+    n_probe = min(Kh.numel(), (1 << 30) // Kh.element_size())
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        for _ in range(2):
+            p0.record(s)
+            Kd.view(-1)[:n_probe].copy_(Kh.view(-1)[:n_probe], non_blocking=True)
+            p1.record(s)
+    torch.cuda.synchronize()
+    link_gbs = n_probe * Kh.element_size() / (p0.elapsed_time(p1) / 1e3) / 1e9
 
     def job():
         ext.record(ev[0], s)
-        ext.copy_prefix_h2d(Kd, Kh, L, s)
+        ext.copy_prefix_h2d_split(Kd, Kh, L, s, k_streams, k_forks, k_joins)
         ext.record(ev[1], s)
         # V is not read before the first decode step: its upload follows K's
         # (the two would share the link) and overlaps the clustering
@@ -875,6 +913,7 @@ def run_e2e(ctx, w, K, V, Q, one_call=False, sync_incremental=False):
     d2h = T * U * g * d * 4
     return {"value": w.batch * T / dt, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "job_s": dt, "phases_ms": {k: round(v, 3) for k, v in phases.items()},
+            "host_link_h2d_gbs": round(link_gbs, 1), "upload_streams": len(k_streams),
             "how": "public API calls recorded once into a CUDA graph and replayed; the prompt K/V, every "
                    "step's q and new K/V rows come from pinned host memory and every step's output goes "
                    "back to it inside the timed replay (V upload overlapping the clustering; " +

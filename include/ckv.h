@@ -380,8 +380,9 @@ ckv_status ckv_set_wait_limit(ckv_ctx* ctx, int64_t cycles, int32_t stall);
  * of the centroids, [units][max_clusters][d], and the label-sorted token ids
  * perm, [units][max_len - sinks] int32), bytes = 0 turns it off.  While it is
  * on, the scoring kernel reads the centroid copy and the selection kernel
- * reads perm through access-policy windows whose hits persist (hit ratio =
- * set-aside / bytes needed, at most 1).  The set-aside is the calling
+ * reads perm through access-policy windows whose hits persist (the centroid
+ * copy's hit ratio = set-aside / its bytes, at most 1; perm's = what is left
+ * of the set-aside / its bytes).  The set-aside is the calling
  * process's CUDA-context limit cudaLimitPersistingL2CacheSize on the current
  * device: it is released with that context, the value found before the first
  * call is restored by bytes = 0 and by ckv_destroy, and the persisting lines

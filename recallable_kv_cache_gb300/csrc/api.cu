@@ -471,8 +471,7 @@ ckv_status ckv_set_l2_persistence(ckv_ctx* ctx, int64_t bytes) {
     const size_t U = (size_t)ctx->cfg.units;
     const size_t mu_bytes = U * ctx->cmax * D * ctx->elem;
     const size_t perm_bytes = U * ctx->ntok * sizeof(int32_t);
-    const size_t need = mu_bytes + perm_bytes;
-    size_t want = bytes < 0 ? need : (size_t)bytes;
+    size_t want = bytes < 0 ? mu_bytes + perm_bytes : (size_t)bytes;
     if (want > (size_t)maxp) want = (size_t)maxp;
     if (!ctx->l2_saved) {
         if ((e = cudaDeviceGetLimit(&ctx->l2_prev_limit, cudaLimitPersistingL2CacheSize)) != cudaSuccess)
@@ -482,9 +481,14 @@ ckv_status ckv_set_l2_persistence(ckv_ctx* ctx, int64_t bytes) {
     if ((e = cudaDeviceSetLimit(cudaLimitPersistingL2CacheSize, want)) != cudaSuccess) return CKV_ERR_CUDA;
     size_t got = 0;
     if ((e = cudaDeviceGetLimit(&got, cudaLimitPersistingL2CacheSize)) != cudaSuccess) return CKV_ERR_CUDA;
-    // both windows share the set-aside: each hit ratio is set-aside / bytes needed
-    const float hit = got >= need ? 1.0f : (float)((double)got / (double)need);
-    auto window = [&](void* base, size_t n) {
+    // the centroid copy first (every step reads all of it), perm from what is
+    // left (a step reads ~B entries of each unit's perm): hit ratio = the part
+    // of each window the set-aside can hold
+    auto ratio = [](size_t have, size_t n) {
+        return have >= n ? 1.0f : (float)((double)have / (double)n);
+    };
+    const size_t left = got > mu_bytes ? got - mu_bytes : 0;
+    auto window = [&](void* base, size_t n, float hit) {
         cudaAccessPolicyWindow w = {};
         w.base_ptr = base;
         w.num_bytes = n < (size_t)maxw ? n : (size_t)maxw;
@@ -493,8 +497,8 @@ ckv_status ckv_set_l2_persistence(ckv_ctx* ctx, int64_t bytes) {
         w.missProp = cudaAccessPropertyStreaming;
         return w;
     };
-    ctx->l2_mu = window(ctx->mu_s, mu_bytes);
-    ctx->l2_perm = window(ctx->perm, perm_bytes);
+    ctx->l2_mu = window(ctx->mu_s, mu_bytes, ratio(got, mu_bytes));
+    ctx->l2_perm = window(ctx->perm, perm_bytes, ratio(left, perm_bytes));
     ctx->l2_on = 1;
     return CKV_OK;
 }

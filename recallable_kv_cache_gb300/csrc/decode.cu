@@ -168,7 +168,7 @@ __device__ __forceinline__ uint64_t rank_key(float s, int c) {
 // shared memory.
 constexpr int SEL_SCORE_UNROLL = 2;
 template <typename T, int G>
-__device__ __forceinline__ void score_unit(const T* __restrict__ q, const T* __restrict__ mu, int u, int cmax,
+__device__ __forceinline__ void score_unit(const uint4* qsm, const T* __restrict__ mu, int u, int cmax,
                                            int C, float* scs, int lane, int warp, int nwarps) {
     constexpr int CPL = Vec<T>::N;   // channels per lane
     constexpr int LPR = D / CPL;     // lanes per centroid row
@@ -180,7 +180,7 @@ __device__ __forceinline__ void score_unit(const T* __restrict__ q, const T* __r
     for (int c = 0; c < CPL; ++c) qs[c] = 0.f;
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-        const uint4 w = *reinterpret_cast<const uint4*>(q + ((size_t)u * G + h) * D + li * CPL);
+        const uint4 w = qsm[(h * D + li * CPL) * (int)sizeof(T) / 16];
         float f[CPL];
         Vec<T>::unpack(w, f);
 #pragma unroll
@@ -251,7 +251,13 @@ __global__ void __launch_bounds__(1024, 1) sel_kernel(
         if constexpr (G == 0) scr[e] = c < C ? scores_in[(size_t)u * sstride + c] : 0.f;
     }
     if constexpr (G > 0) {
-        score_unit<T, G>(q, mu, u, cmax, C, scs, lane, warp, nwarps);
+        // the unit's q (G rows) into shared memory once: every lane needs it,
+        // and q may sit in mapped host memory
+        constexpr int QV = G * D * (int)sizeof(T) / 16;
+        uint4* qsm = reinterpret_cast<uint4*>(scs + N);
+        for (int i = tid; i < QV; i += NT) qsm[i] = reinterpret_cast<const uint4*>(q + (size_t)u * G * D)[i];
+        __syncthreads();
+        score_unit<T, G>(qsm, mu, u, cmax, C, scs, lane, warp, nwarps);
         __syncthreads();
 #pragma unroll
         for (int e = 0; e < E; ++e) {
@@ -1092,7 +1098,8 @@ cudaError_t launch_score_t(const void* q, const void* mu, int g, int units, int 
 template <int E, typename T, int G>
 cudaError_t launch_sel_t(const ckv_ctx* ctx, const float* scores, int stride, const void* q, int C, int N, int B,
                          int32_t* idx, int32_t* count, cudaStream_t s) {
-    // keys, starts, ranks, sizes, offsets; then the histogram (or the scores computed here)
+    // keys, starts, ranks, sizes, offsets; then the histogram (or the scores
+    // computed here followed by q: at most 4 KB, N <= 1024 leaves >= 12 KB)
     const size_t smem = (size_t)N * 24 + (size_t)(N > 4096 ? N : 4096) * 4;
     auto kern = sel_kernel<E, T, G>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
