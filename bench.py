@@ -61,6 +61,11 @@ def parse():
     p.add_argument("--decode-steps", type=int, default=0, help="override the decode steps (profiling)")
     p.add_argument("--sync-incremental", action="store_true",
                    help="cluster the new tokens inline instead of on a side stream overlapping the next step")
+    p.add_argument("--e2e-out-copies", action="store_true",
+                   help="end-to-end run with mapped host memory: each step's output into a device buffer read "
+                        "back while the next step runs, instead of written by the attention straight into pinned "
+                        "host memory (measured slower: with a copy node per step the graph's prompt upload slows "
+                        "down too)")
     p.add_argument("--e2e-copy-nodes", action="store_true",
                    help="end-to-end run: copy each step's inputs and outputs instead of mapping host memory")
     p.add_argument("--upload-streams", type=int, default=K_UPLOAD_STREAMS,
@@ -417,7 +422,7 @@ def run_ours(args, w, rank, world, device):
     res["tensors"] = (K, V, Q)
     if not args.no_e2e:
         res["e2e"] = run_e2e(ctx, w, K, V, Q, one_call, args.sync_incremental, args.upload_streams,
-                             args.e2e_copy_nodes)
+                             args.e2e_copy_nodes, not args.e2e_out_copies)
     return res
 
 
@@ -754,7 +759,7 @@ def full_kv_attention(w, K, V, Q, reps=5):
 
 
 def run_e2e(ctx, w, K, V, Q, one_call=False, sync_incremental=False, upload_streams=K_UPLOAD_STREAMS,
-            copy_nodes=False):
+            copy_nodes=False, out_direct=True):
     """The same job through the public API from pinned host buffers: upload the
     prompt K/V, prefill clustering, then per decode step upload q and the new
     K/V row of every unit, select, attend, and read the output back.  The calls
@@ -763,11 +768,11 @@ def run_e2e(ctx, w, K, V, Q, one_call=False, sync_incremental=False, upload_stre
     Dependencies are those of a real decode loop: the V upload overlaps the
     clustering (which reads K only) after K's.  Where the device maps pinned
     host memory (unified addressing) the step's kernels read q and the new K/V
-    rows from it (ckv_append_kv puts the rows into the caches) and the attention
-    writes the output to it; otherwise a step's q and new K and V rows are
-    copied in parallel when the step starts (the rows straight into the caches
-    by strided copies) and its output is read back on a side stream while the
-    next step runs (two output buffers)."""
+    rows from it (ckv_append_kv puts the rows into the caches); otherwise a
+    step's q and new K and V rows are copied in parallel when the step starts
+    (the rows straight into the caches by strided copies).  The output is read
+    back on a side stream while the next step runs (two device buffers), or
+    with out_direct written by the attention straight into pinned host memory."""
     from recallable_kv_cache_gb300 import ckv
     U, L, B, T, d, g = w.units, w.L, w.B, w.decode_steps, w.d, w.g
     Kh = torch.empty(U, w.max_len, d, dtype=K.dtype, pin_memory=True)
@@ -849,17 +854,38 @@ def run_e2e(ctx, w, K, V, Q, one_call=False, sync_incremental=False, upload_stre
                 ctx.select(q, B, idx, cnt)
                 ctx.sparse_decode_attn(q, Kd, Vd, idx, cnt, B, L + t + 1, out)
 
+        def out_buffer(t):
+            """Where step t's attention writes: the host record itself, or a
+            device buffer (two in turn) read back on a side stream while the
+            next step runs."""
+            if zero_copy and out_direct:
+                return outh[t]
+            if t >= 2:
+                s.wait_event(e_read[t - 2])  # that buffer's read-back is done
+            return outs[t % 2]
+
+        def read_back(t, out):
+            if zero_copy and out_direct:
+                return
+            e_out[t].record(s)
+            dn.wait_event(e_out[t])
+            with torch.cuda.stream(dn):
+                outh[t].copy_(out, non_blocking=True)
+                e_read[t].record(dn)
+
         for t in range(T):
             if zero_copy:
                 # the kernels read this step's q and new K/V rows from pinned host
-                # memory, and the attention writes its output there.  The rows are
-                # read only by the attention: with separate calls they are appended
-                # on a side stream while the scoring and selection run
+                # memory.  The rows are read only by the attention: with separate
+                # calls they are appended on a side stream while the scoring and
+                # selection run
                 q, kh, vh = inp_h[t, :nq].view(U, g, d), inp_h[t, nq:nq + nr].view(U, d), inp_h[t, nq + nr:].view(U, d)
+                out = out_buffer(t)
                 if one_call:
                     ckv.append_kv(kh, vh, Kd, Vd, L + t, stream=s)
                     incremental(t)
-                    decode(t, q, outh[t])
+                    decode(t, q, out)
+                    read_back(t, out)
                     continue
                 e_step[t].record(s)
                 sk.wait_event(e_step[t])
@@ -868,7 +894,8 @@ def run_e2e(ctx, w, K, V, Q, one_call=False, sync_incremental=False, upload_stre
                 incremental(t)
                 ctx.select(q, B, idx, cnt)
                 s.wait_event(e_k[t])
-                ctx.sparse_decode_attn(q, Kd, Vd, idx, cnt, B, L + t + 1, outh[t])
+                ctx.sparse_decode_attn(q, Kd, Vd, idx, cnt, B, L + t + 1, out)
+                read_back(t, out)
                 continue
             # the step's three inputs in parallel: q, and the new K and V rows
             # straight into their place in the caches (one strided copy each)
@@ -883,16 +910,10 @@ def run_e2e(ctx, w, K, V, Q, one_call=False, sync_incremental=False, upload_stre
             s.wait_event(e_k[t])
             s.wait_event(e_vr[t])
             incremental(t)
-            out = outs[t % 2]
-            if t >= 2:
-                s.wait_event(e_read[t - 2])  # that buffer's read-back is done
+            out = out_buffer(t)
             decode(t, qd, out)
-            e_out[t].record(s)
-            dn.wait_event(e_out[t])
-            with torch.cuda.stream(dn):
-                outh[t].copy_(out, non_blocking=True)
-                e_read[t].record(dn)
-        if not zero_copy:
+            read_back(t, out)
+        if not (zero_copy and out_direct):
             s.wait_event(e_read[T - 1])
         ext.record(ev[3], s)
 
@@ -917,10 +938,12 @@ def run_e2e(ctx, w, K, V, Q, one_call=False, sync_incremental=False, upload_stre
             "how": "public API calls recorded once into a CUDA graph and replayed; the prompt K/V, every "
                    "step's q and new K/V rows come from pinned host memory and every step's output goes "
                    "back to it inside the timed replay (V upload overlapping the clustering; " +
-                   ("the step's kernels read q and the new rows from pinned host memory and write the output "
-                    "there" if zero_copy else "the step's three input copies in parallel, outputs read back "
-                    "while the next step runs") + ")",
-            "step_io": "zero-copy (kernels access pinned host memory)" if zero_copy else "copy nodes"}
+                   ("the step's kernels read q and the new rows from pinned host memory" if zero_copy else
+                    "the step's three input copies in parallel") +
+                   ("; the attention writes the output there" if zero_copy and out_direct else
+                    "; outputs read back while the next step runs") + ")",
+            "step_io": ("zero-copy inputs (kernels read pinned host memory)" if zero_copy else "copy nodes") +
+                       (", zero-copy outputs" if zero_copy and out_direct else ", output copies")}
 
 
 # ----------------------------------------------------------------------------- the other workloads

@@ -376,13 +376,15 @@ ckv_status ckv_set_wait_limit(ckv_ctx* ctx, int64_t cycles, int32_t stall);
  * L2; the gathered K/V rows of one step are larger and have no reuse, so
  * without this they evict the rest each step).  bytes > 0 sets aside up to
  * that many bytes of L2 for persisting lines (capped at the device maximum),
- * bytes < 0 sets aside what the context needs (the bf16 / fp32 scoring copy
- * of the centroids, [units][max_clusters][d], and the label-sorted token ids
- * perm, [units][max_len - sinks] int32), bytes = 0 turns it off.  While it is
- * on, the scoring kernel reads the centroid copy and the selection kernel
- * reads perm through access-policy windows whose hits persist (the centroid
- * copy's hit ratio = set-aside / its bytes, at most 1; perm's = what is left
- * of the set-aside / its bytes).  The set-aside is the calling
+ * bytes < 0 sets aside the size of the bf16 / fp32 scoring copy of the
+ * centroids, [units][max_clusters][d], when all of it fits the device's
+ * maximum (and otherwise leaves persistence off: a set-aside holding a
+ * fraction of it would mostly take L2 from the K-means passes), bytes = 0
+ * turns it off.  While it is on, the kernels that score (the selection, up
+ * to 1024 clusters, or the scoring kernel) read the centroid copy through an
+ * access-policy window whose hits persist (hit ratio = set-aside / its
+ * bytes, at most 1), and a selection from given scores reads perm through
+ * one holding what is left of the set-aside.  The set-aside is the calling
  * process's CUDA-context limit cudaLimitPersistingL2CacheSize on the current
  * device: it is released with that context, the value found before the first
  * call is restored by bytes = 0 and by ckv_destroy, and the persisting lines

@@ -471,7 +471,12 @@ ckv_status ckv_set_l2_persistence(ckv_ctx* ctx, int64_t bytes) {
     const size_t U = (size_t)ctx->cfg.units;
     const size_t mu_bytes = U * ctx->cmax * D * ctx->elem;
     const size_t perm_bytes = U * ctx->ntok * sizeof(int32_t);
-    size_t want = bytes < 0 ? mu_bytes + perm_bytes : (size_t)bytes;
+    // what the context needs: the centroid copy (a selection that scores its
+    // own unit reads only it through its window), and only when all of it
+    // fits: a partial set-aside keeps little of it and takes L2 from the
+    // K-means passes
+    if (bytes < 0 && mu_bytes > (size_t)maxp) return cuda_status(l2_release(ctx));
+    size_t want = bytes < 0 ? mu_bytes : (size_t)bytes;
     if (want > (size_t)maxp) want = (size_t)maxp;
     if (!ctx->l2_saved) {
         if ((e = cudaDeviceGetLimit(&ctx->l2_prev_limit, cudaLimitPersistingL2CacheSize)) != cudaSuccess)
