@@ -39,8 +39,10 @@ METRIC = "sparse-decode tokens/s at 32k ctx, B=1024; K-means ms/layer; % of HBM 
 # algorithmic byte, from one ncu capture of the current kernels on a 64-unit
 # case; the traffic of a full-size step is this ratio times its algorithmic
 # bytes.  None whenever a kernel changes until it is captured again.
-STEP_TRAFFIC_PER_ALG_BYTE = None
-STEP_TRAFFIC_SOURCE = "not captured for the current kernels"
+STEP_TRAFFIC_PER_ALG_BYTE = 45.19e6 / 42.46e6
+STEP_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of the four kernels of one decode step, "
+                       "64-unit case (caches flushed between kernels), scaled by algorithmic bytes "
+                       "(profiles/decode_step_traffic_decode_32k.md)")
 WORKLOAD = "decode_32k"
 K_UPLOAD_STREAMS = 1  # the prompt's keys go up in this many concurrent copies
 
