@@ -89,6 +89,47 @@ def test_select_equals_score_then_select(case):
     assert torch.equal(c1, c2) and torch.equal(i1, i2)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("g", [1, 2, 8])
+def test_select_scores_its_units_for_every_group_size(dtype, g):
+    """Up to 1024 clusters each selection CTA scores its own unit (one kernel
+    instance per key dtype and group size): ckv_select equals ckv_score +
+    ckv_select_scored bit for bit, and the selection from those scores equals
+    the oracle's; random cluster layouts (empty clusters included)."""
+    torch.cuda.init()
+    U, C, n, d = 3, 45, 600, 128
+    L = 16 + n
+    rng = np.random.default_rng(77 + g + (0 if dtype == "bf16" else 100))
+    ctx = make_ctx(U, g, L + 8, C, 1024, dtype)
+    states = []
+    for u in range(U):
+        labels = rng.integers(0, C, size=n)
+        labels[labels % 7 == 3] = 0  # some clusters stay empty
+        sizes, offsets, perm = ck.build_csr(labels, C, 16)
+        mu = rng.standard_normal((C, d)).astype(np.float32).astype(np.float64)
+        states.append(dict(mu=mu, sizes=sizes, offsets=offsets, perm=perm))
+    upload_state(ctx, states, L)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    q = torch.from_numpy(rng.standard_normal((U, g, d))).to(tdt).cuda().contiguous()
+    sc = torch.empty(U, C, dtype=torch.float32, device="cuda")
+    ctx.score(q, sc)
+    for B in (1, 100, 599, 1024):
+        i1 = torch.full((U, B), -2, dtype=torch.int32, device="cuda")
+        c1 = torch.empty(U, dtype=torch.int32, device="cuda")
+        i2, c2 = torch.full_like(i1, -2), torch.empty_like(c1)
+        ctx.select_scored(sc, B, i1, c1)
+        ctx.select(q, B, i2, c2)
+        torch.cuda.synchronize()
+        assert ctx.device_error() == 0
+        assert torch.equal(c1, c2) and torch.equal(i1, i2)
+        got_i, got_c, s64 = i2.cpu().numpy(), c2.cpu().numpy(), to64(sc)
+        for u in range(U):
+            st = states[u]
+            want, wc = ck.select(s64[u], st["sizes"], st["offsets"], st["perm"], B)
+            assert got_c[u] == wc and np.array_equal(got_i[u, :wc], want)
+    ctx.close()
+
+
 @pytest.mark.parametrize("pending", [0, 1, "case"])
 def test_attention_given_idx(case, pending):
     w, ctx = case["w"], case["ctx"]
