@@ -1,14 +1,15 @@
 // Decode-step kernels of the ClusterKV path:
 //   score_kernel   cluster scores q . mu (section "Selection at semantic-cluster
-//                  granularity"), HBM-bound stream over the centroid table;
+//                  granularity"), a many-CTA stream over the centroid table
+//                  (above 1024 clusters, and for ckv_score);
 //   sel_kernel     (scores of the unit's clusters, up to 1024 of them,) rank
 //                  clusters, prefix-sum their sizes, trim the last one and
 //                  compact the token ids (section "Selection and indexing
 //                  mechanism", Fig. 8), one CTA per unit;
-//   attn_kernel    gather of the selected K/V rows with bulk-async copies into
-//                  shared memory and split-K flash-decode attention (section
-//                  "Background": softmax(q K_S^T / sqrt(d)) V_S), with the
-//                  cross-split combine done by the last CTA of each unit.
+//   attn_kernel    fp32 K/V: gather of the selected rows with bulk-async
+//                  copies into shared memory and split-K flash-decode attention
+//                  (section "Background": softmax(q K_S^T / sqrt(d)) V_S);
+//                  attn_combine_kernel merges the split partials.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -149,16 +150,6 @@ __device__ __forceinline__ uint64_t rank_key(float s, int c) {
     return ((uint64_t)(~ord) << 32) | (uint32_t)c;                      // descending score, asc c
 }
 
-// One CTA per unit.  Scores (computed by the CTA itself from q and the
-// centroid copy up to 1024 clusters, else from score_kernel or the caller)
-// become 64-bit keys (descending score, ascending cluster index) that are sorted by a
-// bitonic network held in registers: exchange distances below 32 use warp
-// shuffles, larger ones shared memory, and distances of at least the block
-// size stay inside a thread (E keys per thread).  The sizes taken in rank
-// order are prefix-summed, the budget cut found, and every output slot
-// p < min(B, total) looks up its rank by binary search and copies its token id
-// from the label-sorted permutation.  The sizes, offsets and scores are all
-// loaded before any of them is used, so they share one round trip.
 // Scores of every cluster of unit u computed inside the selection's CTA
 // (the same arithmetic as score_kernel, so the same bits): q summed over the
 // g heads, then per centroid row LPR lanes take CPL channels each (fma chain
@@ -217,6 +208,18 @@ __device__ __forceinline__ void score_unit(const uint4* qsm, const T* __restrict
     }
 }
 
+// One CTA per unit.  Scores (computed by the CTA itself from q and the
+// centroid copy up to 1024 clusters, else from score_kernel or the caller)
+// become 64-bit keys (descending score, ascending cluster index) that are sorted by a
+// bitonic network held in registers: exchange distances below 32 use warp
+// shuffles, larger ones shared memory, and distances of at least the block
+// size stay inside a thread (E keys per thread).  The sizes taken in rank
+// order are prefix-summed, the budget cut found, and every output slot
+// p < min(B, total) looks up its rank by binary search and copies its token id
+// from the label-sorted permutation.  The sizes and offsets (and given
+// scores) are loaded before any of them is used, so they share one round
+// trip, which the scoring overlaps.
+//
 // G == 0: scores_in [units][sstride] are given.  G > 0: the scores are
 // computed here from q [units][G][D] and the scoring copy mu [units][cmax][D]
 // of type T.
