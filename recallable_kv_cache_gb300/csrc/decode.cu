@@ -156,7 +156,9 @@ __device__ __forceinline__ uint64_t rank_key(float s, int c) {
 // in channel order) and a shuffle reduction over the row's lanes.  Rows are
 // read in rounds of SEL_SCORE_UNROLL rows per lane group, the next round's
 // loads in flight while the current one is reduced; the scores land in
-// shared memory.
+// shared memory.  The first round's loads are issued before the barrier that
+// publishes the staged q (they do not depend on it), so the two round trips
+// overlap; every thread of the CTA calls this.
 constexpr int SEL_SCORE_UNROLL = 2;
 template <typename T, int G>
 __device__ __forceinline__ void score_unit(const uint4* qsm, const T* __restrict__ mu, int u, int cmax,
@@ -166,17 +168,6 @@ __device__ __forceinline__ void score_unit(const uint4* qsm, const T* __restrict
     constexpr int RPI = 32 / LPR;    // rows per warp-wide load
     constexpr int UN = SEL_SCORE_UNROLL;
     const int sub = lane / LPR, li = lane % LPR;
-    float qs[CPL];
-#pragma unroll
-    for (int c = 0; c < CPL; ++c) qs[c] = 0.f;
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-        const uint4 w = qsm[(h * D + li * CPL) * (int)sizeof(T) / 16];
-        float f[CPL];
-        Vec<T>::unpack(w, f);
-#pragma unroll
-        for (int c = 0; c < CPL; ++c) qs[c] += f[c];
-    }
     const T* mu_u = mu + (size_t)u * cmax * D + li * CPL;
     const int per_round = nwarps * RPI * UN;
     auto row_of = [&](int r0, int i) { return r0 + (i * nwarps + warp) * RPI + sub; };
@@ -189,6 +180,18 @@ __device__ __forceinline__ void score_unit(const uint4* qsm, const T* __restrict
     };
     uint4 cur[UN], nxt[UN];
     load(0, cur);
+    __syncthreads();  // q staged in qsm
+    float qs[CPL];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) qs[c] = 0.f;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        const uint4 w = qsm[(h * D + li * CPL) * (int)sizeof(T) / 16];
+        float f[CPL];
+        Vec<T>::unpack(w, f);
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) qs[c] += f[c];
+    }
     for (int r0 = 0; r0 < C; r0 += per_round) {
         if (r0 + per_round < C) load(r0 + per_round, nxt);
 #pragma unroll
@@ -259,8 +262,7 @@ __global__ void __launch_bounds__(1024, 1) sel_kernel(
         constexpr int QV = G * D * (int)sizeof(T) / 16;
         uint4* qsm = reinterpret_cast<uint4*>(scs + N);
         for (int i = tid; i < QV; i += NT) qsm[i] = reinterpret_cast<const uint4*>(q + (size_t)u * G * D)[i];
-        __syncthreads();
-        score_unit<T, G>(qsm, mu, u, cmax, C, scs, lane, warp, nwarps);
+        score_unit<T, G>(qsm, mu, u, cmax, C, scs, lane, warp, nwarps);  // its first barrier publishes qsm
         __syncthreads();
 #pragma unroll
         for (int e = 0; e < E; ++e) {
