@@ -155,14 +155,16 @@ __device__ __forceinline__ uint64_t rank_key(float s, int c) {
 // g heads, then per centroid row LPR lanes take CPL channels each (fma chain
 // in channel order) and a shuffle reduction over the row's lanes.  Rows are
 // read in rounds of SEL_SCORE_UNROLL rows per lane group, the next round's
-// loads in flight while the current one is reduced; the scores land in
-// shared memory.  The first round's loads are issued before the barrier that
-// publishes the staged q (they do not depend on it), so the two round trips
-// overlap; every thread of the CTA calls this.
+// loads in flight while the current one is reduced.  A warp scores at most 32
+// rows (C <= N, rounds of nwarps * 2 * UN rows): lane j of the warp keeps
+// the rank key of the warp's j-th row (~0 past the last), which the caller
+// sorts in registers.  The first round's loads are issued before the barrier
+// that publishes the staged q (they do not depend on it), so the two round
+// trips overlap; every thread of the CTA calls this.
 constexpr int SEL_SCORE_UNROLL = 2;
 template <typename T, int G>
-__device__ __forceinline__ void score_unit(const uint4* qsm, const T* __restrict__ mu, int u, int cmax,
-                                           int C, float* scs, int lane, int warp, int nwarps) {
+__device__ __forceinline__ uint64_t score_unit(const uint4* qsm, const T* __restrict__ mu, int u, int cmax,
+                                               int C, int lane, int warp, int nwarps) {
     constexpr int CPL = Vec<T>::N;   // channels per lane
     constexpr int LPR = D / CPL;     // lanes per centroid row
     constexpr int RPI = 32 / LPR;    // rows per warp-wide load
@@ -192,10 +194,13 @@ __device__ __forceinline__ void score_unit(const uint4* qsm, const T* __restrict
 #pragma unroll
         for (int c = 0; c < CPL; ++c) qs[c] += f[c];
     }
+    // this warp's j-th row: round j / (RPI * UN), i = (j / RPI) % UN, sub = j % RPI
+    uint64_t key = ~0ull;
+    int it = 0;  // (round, i) in order
     for (int r0 = 0; r0 < C; r0 += per_round) {
         if (r0 + per_round < C) load(r0 + per_round, nxt);
 #pragma unroll
-        for (int i = 0; i < UN; ++i) {
+        for (int i = 0; i < UN; ++i, ++it) {
             float f[CPL];
             Vec<T>::unpack(cur[i], f);
             float dot = 0.f;
@@ -203,12 +208,16 @@ __device__ __forceinline__ void score_unit(const uint4* qsm, const T* __restrict
             for (int c = 0; c < CPL; ++c) dot = fmaf(qs[c], f[c], dot);
 #pragma unroll
             for (int o = LPR / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(FULL, dot, o);
-            const int r = row_of(r0, i);
-            if (li == 0 && r < C) scs[r] = dot;
+            // every lane of a row's lane group holds its sum: lane j takes the
+            // sum of the row with sub = j % RPI from that group's first lane
+            const float mine = __shfl_sync(FULL, dot, (lane % RPI) * LPR);
+            const int r = r0 + (i * nwarps + warp) * RPI + lane % RPI;
+            if (lane / RPI == it && r < C) key = rank_key(mine, r);
         }
 #pragma unroll
         for (int i = 0; i < UN; ++i) cur[i] = nxt[i];
     }
+    return key;
 }
 
 // One CTA per unit.  Scores (computed by the CTA itself from q and the
@@ -256,36 +265,39 @@ __global__ void __launch_bounds__(1024, 1) sel_kernel(
         ofr[e] = c < C ? offsets[(size_t)u * (cmax + 1) + c] : 0;
         if constexpr (G == 0) scr[e] = c < C ? scores_in[(size_t)u * sstride + c] : 0.f;
     }
+    uint64_t wkey = ~0ull;  // scored here: this lane's key among its warp's rows
     if constexpr (G > 0) {
+        static_assert(E == 1, "scoring in the selection uses one key slot per thread");
         // the unit's q (G rows) into shared memory once: every lane needs it,
         // and q may sit in mapped host memory
         constexpr int QV = G * D * (int)sizeof(T) / 16;
         uint4* qsm = reinterpret_cast<uint4*>(scs + N);
         for (int i = tid; i < QV; i += NT) qsm[i] = reinterpret_cast<const uint4*>(q + (size_t)u * G * D)[i];
-        score_unit<T, G>(qsm, mu, u, cmax, C, scs, lane, warp, nwarps);  // its first barrier publishes qsm
-        __syncthreads();
+        wkey = score_unit<T, G>(qsm, mu, u, cmax, C, lane, warp, nwarps);  // its first barrier publishes qsm
+    }
+    // ---- 2. unsorted keys (N is a multiple of NT: every slot is written).
+    // Given scores: slot c holds cluster c's key.  Scored here: slot 32 w + j
+    // holds the key of warp w's j-th row.  Either order serves: every later
+    // step takes the cluster from the key; unused slots hold ~0.
+    if constexpr (G > 0) {
+        sk[tid] = wkey;
+    } else {
 #pragma unroll
         for (int e = 0; e < E; ++e) {
             const int c = e * NT + tid;
-            scr[e] = c < C ? scs[c] : 0.f;
+            sk[c] = c < C ? rank_key(scr[e], c) : ~0ull;
         }
-    }
-    // ---- 2. unsorted keys (N is a multiple of NT: every slot is written)
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-        const int c = e * NT + tid;
-        sk[c] = c < C ? rank_key(scr[e], c) : ~0ull;
     }
 #pragma unroll
     for (int e = 0; e < E; ++e) {
         szc[e * NT + tid] = szr[e];
         offc[e * NT + tid] = ofr[e];
     }
-    __syncthreads();
 
     // ---- 3. fast path: the 32 highest-ranked clusters.  Warp w sorts the E
     // lists of 32 keys it owns (in registers; sk keeps its order) and merges
-    // them into its 32 smallest keys; then a merge tree across the warps: at
+    // them into its 32 smallest keys (scored here: straight from the scoring's
+    // registers, before the barrier); then a merge tree across the warps: at
     // each level the lower half of the remaining lists takes in the upper
     // half (one merge per warp, all warps of a level at once), while the last
     // warp sums the sizes.  If those 32 clusters hold min(B, total) tokens,
@@ -293,14 +305,18 @@ __global__ void __launch_bounds__(1024, 1) sel_kernel(
     // needed.
     __shared__ int s_fast, s_nsel, s_total;
     uint64_t* part = reinterpret_cast<uint64_t*>(start);  // [nwarps][32] (start/cl reused)
-    {
+    if constexpr (G > 0) {
+        part[32 * warp + lane] = warp_sort32(wkey, lane);
+        __syncthreads();  // sk, szc, offc and part
+    } else {
+        __syncthreads();  // sk, szc, offc
         uint64_t top = warp_sort32(sk[32 * warp + lane], lane);
 #pragma unroll
         for (int e = 1; e < E; ++e)
             top = warp_merge32(top, warp_sort32(sk[32 * (warp + e * nwarps) + lane], lane), lane);
         part[32 * warp + lane] = top;
+        __syncthreads();
     }
-    __syncthreads();
     if (warp == nwarps - 1) {  // never merges: nwarps >= 4, the tree's warps are below nwarps / 2
         int tot = 0;  // clustered tokens: the sum of all sizes
         for (int c = lane; c < C; c += 32) tot += szc[c];
@@ -360,7 +376,10 @@ __global__ void __launch_bounds__(1024, 1) sel_kernel(
     for (int i = tid; i < NBIN; i += NT) hist[i] = 0;
     if (tid == 0) s_M = 0;
     __syncthreads();
-    for (int c = tid; c < C; c += NT) atomicAdd(&hist[(int)(sk[c] >> (64 - HBITS))], szc[c]);
+    for (int i = tid; i < N; i += NT) {
+        const uint64_t k = sk[i];
+        if (k != ~0ull) atomicAdd(&hist[(int)(k >> (64 - HBITS))], szc[(int)(uint32_t)k]);
+    }
     __syncthreads();
     {
         // block-wide: thread t owns bins [t*PER, t*PER + PER) (NT * PER == NBIN)
@@ -407,16 +426,16 @@ __global__ void __launch_bounds__(1024, 1) sel_kernel(
     // every cluster needs ranking when the budget covers all tokens
     const bool take_all = total <= B;
     if (!take_all) {
-        for (int c0 = 0; c0 < C; c0 += NT) {  // c0 is warp-uniform: the ballot sees all lanes
-            const int c = c0 + tid;
-            const bool is_c = c < C && (int)(sk[c] >> (64 - HBITS)) <= bstar;
+        for (int i0 = 0; i0 < N; i0 += NT) {  // i0 is warp-uniform: the ballot sees all lanes
+            const uint64_t k = sk[i0 + tid];
+            const bool is_c = k != ~0ull && (int)(k >> (64 - HBITS)) <= bstar;
             const unsigned bal = __ballot_sync(FULL, is_c);
             int wbase = 0;
             if (lane == 0 && bal) wbase = atomicAdd(&s_M, __popc(bal));
             wbase = __shfl_sync(FULL, wbase, 0);
             if (is_c) {
                 const int pos = wbase + __popc(bal & ((1u << lane) - 1u));
-                if (pos < NT) cand[pos] = sk[c];
+                if (pos < NT) cand[pos] = k;
             }
         }
     }
